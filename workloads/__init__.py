@@ -1,0 +1,228 @@
+"""Seeded synthetic inputs for sparse MLA decode over a paged FP8 KV cache.
+
+This module builds INPUTS only.  It holds none of the attention arithmetic; the CUDA
+library and the CPU oracle both consume what it makes, and neither is imported here.
+
+Row format ("FlashMLA 与 DSA：内核、流水线和正确性边界", section 3.1; "FlashMLA Sparse
+Decode 完整计算过程详解", steps 2.2, 4.2 and 4.3): 656 bytes per token = 512 e4m3 codes of
+the NoPE part, 4 little-endian fp32 scales (one per 128-dim group; the stored value is
+the dequant multiplier), 64 bf16 RoPE values stored as is.
+
+Quantiser (input preparation, step 4.2 of the second page): per 128-dim group,
+``scale = amax / 448`` in fp32, or the power of two ``2^ceil(log2(amax / 448))`` for
+ue8m0-style scales; ``code = rn_e4m3(x / scale)`` with the quotient in fp32, saturated to
++-448; an all-zero group gets scale 1.
+
+Indices are physical token ids ``page * 64 + offset`` reached through a per-sequence page
+table whose pages are scattered at random over a shared pool.
+
+The five benchmark workloads (``CONFIGS``) follow the configuration list this project is
+measured on; ``seed`` is the config's position 0..4.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+D_NOPE, D_ROPE, D_QK, D_V = 512, 64, 576, 512
+GROUP = 128
+ROW_BYTES = 656
+PAGE = 64
+E4M3_MAX = 448.0
+
+
+@dataclass
+class Spec:
+    name: str
+    b: int
+    s_q: int
+    h_q: int
+    topk: int
+    ctx: int  # tokens per sequence
+    ue8m0: bool = False
+    masked_per_row: int = 0  # exactly this many slots per row set to -1
+    causal_base: int | None = None  # query token i sees positions [0, causal_base + i]
+    sort_indices: bool = False  # sort each row ascending by physical id
+    extra_pool_pages: int = 0
+    seed: int = 0
+
+    @property
+    def pages_per_seq(self) -> int:
+        return -(-self.ctx // PAGE)
+
+    @property
+    def num_blocks(self) -> int:
+        return self.b * self.pages_per_seq + self.extra_pool_pages
+
+
+CONFIGS: dict[str, Spec] = {
+    # b=2, s_q=1, h=128, topk=128, 4096-token context per sequence.
+    "c1_b2_h128_k128": Spec("c1_b2_h128_k128", b=2, s_q=1, h_q=128, topk=128, ctx=4096, seed=0),
+    # b=64, h=128, topk=2048, 32768-token context, 5% (102) slots per row masked.
+    "c2_b64_h128_k2048_mask5": Spec("c2_b64_h128_k2048_mask5", b=64, s_q=1, h_q=128,
+                                    topk=2048, ctx=32768, masked_per_row=102, seed=1),
+    # h=64, b=128, s_q=2 (multi-token decode), 65536-token context, causal prefix.
+    "c3_b128_sq2_h64_k2048": Spec("c3_b128_sq2_h64_k2048", b=128, s_q=2, h_q=64, topk=2048,
+                                  ctx=65536, causal_base=65534, seed=2),
+    # ue8m0 power-of-two scales, b=32, 131072-token context; sorted and permuted indices.
+    "c4_b32_h128_k2048_ue8m0_sorted": Spec("c4_b32_h128_k2048_ue8m0_sorted", b=32, s_q=1,
+                                           h_q=128, topk=2048, ctx=131072, ue8m0=True,
+                                           sort_indices=True, seed=3),
+    "c4_b32_h128_k2048_ue8m0_perm": Spec("c4_b32_h128_k2048_ue8m0_perm", b=32, s_q=1,
+                                         h_q=128, topk=2048, ctx=131072, ue8m0=True, seed=3),
+    # prefill-shaped: b=1, s_q=4096, h=128, topk=2048 from a 65536-token context, causal
+    # (query i sees [0, 61440 + i]).
+    "c5_b1_sq4096_h128_k2048": Spec("c5_b1_sq4096_h128_k2048", b=1, s_q=4096, h_q=128,
+                                    topk=2048, ctx=65536, causal_base=61440, seed=4),
+}
+
+
+@dataclass
+class Workload:
+    spec: Spec
+    q: torch.Tensor  # bf16 [b, s_q, h_q, 576]
+    kv: torch.Tensor  # uint8 [num_blocks, 64, 1, 656]
+    indices: torch.Tensor  # int32 [b, s_q, topk]
+    block_table: torch.Tensor  # int32 [b, pages_per_seq]
+    sm_scale: float
+    extras: dict = field(default_factory=dict)
+
+    @property
+    def num_valid(self) -> int:
+        nb = self.kv.shape[0] * PAGE
+        i = self.indices
+        return int(((i >= 0) & (i < nb)).sum().item())
+
+
+def ue8m0_scale(amax_over_max: torch.Tensor) -> torch.Tensor:
+    """2^ceil(log2(v)) for positive fp32 v, exactly (via frexp)."""
+    m, e = torch.frexp(amax_over_max)
+    e = torch.where(m == 0.5, e - 1, e)
+    return torch.ldexp(torch.ones_like(amax_over_max), e)
+
+
+def quantize_rows(x: torch.Tensor, ue8m0: bool = False) -> torch.Tensor:
+    """bf16 [N, 576] -> uint8 [N, 656] in the FP8 row format."""
+    assert x.dtype == torch.bfloat16 and x.shape[-1] == D_QK
+    n = x.shape[0]
+    nope = x[:, :D_NOPE].float().view(n, D_NOPE // GROUP, GROUP)
+    amax = nope.abs().amax(dim=-1)
+    ratio = amax / E4M3_MAX
+    scale = ue8m0_scale(ratio) if ue8m0 else ratio
+    scale = torch.where(amax == 0, torch.ones_like(scale), scale).float()
+    q = (nope / scale[..., None]).clamp_(-E4M3_MAX, E4M3_MAX)
+    codes = q.to(torch.float8_e4m3fn).view(torch.uint8).view(n, D_NOPE)
+    out = torch.empty(n, ROW_BYTES, dtype=torch.uint8, device=x.device)
+    out[:, :D_NOPE] = codes
+    out[:, D_NOPE:D_NOPE + 16] = scale.contiguous().view(torch.uint8).view(n, 16)
+    out[:, D_NOPE + 16:] = x[:, D_NOPE:].contiguous().view(torch.uint8).view(n, 2 * D_ROPE)
+    return out
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def make_pool(num_blocks: int, ue8m0: bool, gen: torch.Generator, device,
+              chunk_rows: int = 1 << 20) -> torch.Tensor:
+    rows = num_blocks * PAGE
+    kv = torch.empty(rows, ROW_BYTES, dtype=torch.uint8, device=device)
+    for lo in range(0, rows, chunk_rows):
+        hi = min(rows, lo + chunk_rows)
+        x = torch.randn(hi - lo, D_QK, generator=gen, device=device).to(torch.bfloat16)
+        kv[lo:hi] = quantize_rows(x, ue8m0)
+    return kv.view(num_blocks, PAGE, 1, ROW_BYTES)
+
+
+def sample_distinct(rows: int, limits: torch.Tensor, k: int, gen: torch.Generator,
+                    device) -> torch.Tensor:
+    """k distinct positions per row, uniform over [0, limits[row]) (in random order)."""
+    maxlim = int(limits.max().item())
+    out = torch.empty(rows, k, dtype=torch.int64, device=device)
+    step = max(1, (1 << 27) // max(maxlim, 1))
+    for lo in range(0, rows, step):
+        hi = min(rows, lo + step)
+        keys = torch.rand(hi - lo, maxlim, generator=gen, device=device)
+        pos = torch.arange(maxlim, device=device)[None, :]
+        keys = torch.where(pos < limits[lo:hi, None], keys, torch.full_like(keys, 2.0))
+        out[lo:hi] = torch.topk(keys, k, dim=1, largest=False, sorted=True).indices
+    return out
+
+
+def logical_to_physical(pos: torch.Tensor, block_table: torch.Tensor,
+                        seq_of_row: torch.Tensor) -> torch.Tensor:
+    page = block_table[seq_of_row[:, None], pos // PAGE].long()
+    return page * PAGE + pos % PAGE
+
+
+def make(spec: Spec, device="cpu", gen_device=None) -> Workload:
+    """Build the workload for ``spec`` deterministically from ``spec.seed``."""
+    device = torch.device(device)
+    gd = torch.device(gen_device) if gen_device is not None else device
+    gen = _gen(gd, spec.seed)
+    b, s_q, h, k = spec.b, spec.s_q, spec.h_q, spec.topk
+    q = torch.randn(b, s_q, h, D_QK, generator=gen, device=gd).to(torch.bfloat16)
+    kv = make_pool(spec.num_blocks, spec.ue8m0, gen, gd)
+    perm = torch.randperm(spec.num_blocks, generator=gen, device=gd)
+    block_table = perm[: b * spec.pages_per_seq].view(b, spec.pages_per_seq).to(torch.int32)
+    rows = b * s_q
+    seq_of_row = torch.arange(b, device=gd).repeat_interleave(s_q)
+    if spec.causal_base is not None:
+        qi = torch.arange(s_q, device=gd).repeat(b)
+        limits = torch.clamp(spec.causal_base + qi + 1, max=spec.ctx)
+    else:
+        limits = torch.full((rows,), spec.ctx, dtype=torch.int64, device=gd)
+    kk = min(k, int(limits.min().item()))
+    pos = sample_distinct(rows, limits, kk, gen, gd)
+    phys = logical_to_physical(pos, block_table, seq_of_row)
+    if kk < k:  # a row shorter than topk is padded with -1 at the end
+        pad = torch.full((rows, k - kk), -1, dtype=phys.dtype, device=gd)
+        phys = torch.cat([phys, pad], dim=1)
+    if spec.sort_indices:
+        phys = torch.sort(phys, dim=1).values
+    if spec.masked_per_row:
+        which = torch.topk(torch.rand(rows, k, generator=gen, device=gd), spec.masked_per_row,
+                           dim=1).indices
+        phys = phys.scatter(1, which, -1)
+    indices = phys.to(torch.int32).view(b, s_q, k)
+    wl = Workload(spec, q.to(device), kv.to(device), indices.to(device),
+                  block_table.to(device), 1.0 / math.sqrt(D_QK))
+    return wl
+
+
+def small(b=2, s_q=1, h_q=128, topk=128, ctx=512, ue8m0=False, masked_per_row=0,
+          causal_base=None, sort_indices=False, extra_pool_pages=0, seed=0,
+          device="cpu") -> Workload:
+    """A scaled-down workload with the same structure (for parity tests)."""
+    spec = Spec(f"small_b{b}_sq{s_q}_h{h_q}_k{topk}_ctx{ctx}", b=b, s_q=s_q, h_q=h_q,
+                topk=topk, ctx=ctx, ue8m0=ue8m0, masked_per_row=masked_per_row,
+                causal_base=causal_base, sort_indices=sort_indices,
+                extra_pool_pages=extra_pool_pages, seed=seed)
+    return make(spec, device=device)
+
+
+def to_numpy_inputs(wl: Workload):
+    """(q as uint16 bf16 bits, kv uint8, indices int32) numpy arrays on the host."""
+    q = wl.q.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+    kv = wl.kv.detach().cpu().contiguous().numpy()
+    kv = kv.reshape(kv.shape[0], kv.shape[1], ROW_BYTES)
+    idx = wl.indices.detach().cpu().contiguous().numpy()
+    return q, kv, idx
+
+
+def flops_valid(wl: Workload) -> float:
+    """Algorithmic FLOPs: 2 * h * (576 + 512) per valid slot (an FMA counts 2)."""
+    return 2.0 * wl.spec.h_q * (D_QK + D_V) * wl.num_valid
+
+
+def alg_bytes(wl: Workload) -> float:
+    """Algorithmic HBM bytes: gathered rows + Q + O + indices + LSE per query token."""
+    tok = wl.spec.b * wl.spec.s_q
+    h = wl.spec.h_q
+    return (wl.num_valid * ROW_BYTES + tok * (h * D_QK * 2 + h * D_V * 2 + wl.spec.topk * 4
+                                              + h * 4))
