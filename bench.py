@@ -1,0 +1,383 @@
+"""Benchmark: sparse MLA decode on GB300 (TFLOPS, gathered KV tokens/s, fraction of roofline).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = the whole hot path on one batch: split-KV plan (sched_meta), decode pass, combine,
+all through the C ABI, inputs resident in HBM.  L2 is flushed (a 256 MiB write) between
+steps; the flush is outside the step time.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload (the reference arm of this project: the pages ship no runnable code).
+Under torchrun (N > 1) every rank runs an independent replica of the workload on its own GPU
+(no collective on the data path) and the job value is the sum of work over the max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse MLA decode TFLOPS & gathered KV tokens/s, % of roofline (1×GB300)"
+DEFAULT_WORKLOAD = "c2_b64_h128_k2048_mask5"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def traffic_from_profiles(kernel_src: str, workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, or None when the summary
+    is missing, is for another workload, or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path, encoding="utf-8").read()
+    m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_src or not m_b:
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if m_src.group(1) == sha else None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def compact_for_oracle(wl, tokens):
+    """Inputs restricted to ``tokens`` with the rows they select gathered into a small pool
+    (indices renumbered, invalid slots kept invalid), as numpy arrays for the oracle."""
+    import numpy as np
+    import torch
+    b, s_q, h = wl.spec.b, wl.spec.s_q, wl.spec.h_q
+    nrows = wl.kv.shape[0] * 64
+    t = torch.as_tensor(tokens, device=wl.indices.device)
+    idx = wl.indices.view(b * s_q, -1)[t].long()
+    valid = (idx >= 0) & (idx < nrows)
+    used = torch.unique(idx[valid])
+    remap = torch.full((nrows,), -1, dtype=torch.int64, device=idx.device)
+    remap[used] = torch.arange(used.numel(), device=idx.device)
+    new_idx = torch.where(valid, remap[idx.clamp(0, nrows - 1)], torch.full_like(idx, -1))
+    pool = torch.zeros(max((used.numel() + 63) // 64, 1) * 64, 656, dtype=torch.uint8,
+                       device=idx.device)
+    pool[: used.numel()] = wl.kv.view(nrows, 656)[used]
+    n = len(tokens)
+    q = wl.q.view(b * s_q, h, 576)[t].cpu().contiguous().view(torch.int16).numpy().view("uint16")
+    return (q.reshape(n, 1, h, 576), pool.cpu().numpy().reshape(-1, 64, 656),
+            new_idx.to(torch.int32).cpu().numpy().reshape(n, 1, -1),
+            int(valid.sum().item()))
+
+
+def time_oracle(wl, budget_s: float, max_tokens: int | None = None):
+    """Run the oracle over query tokens until ``budget_s`` of CPU time is spent."""
+    import oracle
+    import workloads
+    n_tok = wl.spec.b * wl.spec.s_q
+    chunk = 4
+    done, valid, elapsed = 0, 0, 0.0
+    limit = n_tok if max_tokens is None else min(n_tok, max_tokens)
+    while done < limit and elapsed < budget_s:
+        toks = list(range(done, min(limit, done + chunk)))
+        q, kv, idx, nv = compact_for_oracle(wl, toks)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale)
+        elapsed += time.perf_counter() - t0
+        done += len(toks)
+        valid += nv
+    flops = 2.0 * wl.spec.h_q * (workloads.D_QK + workloads.D_V) * valid
+    return {"flops": flops, "seconds": elapsed, "tokens": done, "valid_slots": valid,
+            "threads": oracle.max_threads()}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import workloads
+    import oracle
+    oracle.build()
+    spec = workloads.CONFIGS[args.workload]
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    wl = workloads.make(spec, device=dev)
+    per_step_tokens = max(1, min(spec.b * spec.s_q, args.ref_tokens))
+    for _ in range(args.warmup):
+        time_oracle(wl, 1e9, max_tokens=per_step_tokens)
+    secs, flops, valid = [], 0.0, 0
+    for _ in range(args.steps):
+        r = time_oracle(wl, 1e9, max_tokens=per_step_tokens)
+        secs.append(r["seconds"])
+        flops += r["flops"]
+        valid += r["valid_slots"]
+    total = sum(secs)
+    tflops = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
+                   "topk": spec.topk, "ctx": spec.ctx,
+                   "sample": f"first {per_step_tokens} query tokens per step"},
+        "gathered_tokens_per_s": valid / total,
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step_tokens} of {spec.b * spec.s_q} query tokens of "
+                                   f"{spec.name} per step, all heads"},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the cpu_baseline leg")
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    import sparse_mla_attention_decode_gb300 as smla
+    import workloads
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    smla.lib()
+    spec = workloads.CONFIGS[args.workload]
+    wl = workloads.make(spec, device=dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    op = smla.SparseMLADecode(spec.b, spec.s_q, spec.h_q, spec.topk, wl.kv.shape[0], device=dev,
+                              num_sms=num_sms)
+    out = torch.empty(spec.b, spec.s_q, spec.h_q, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(spec.b, spec.h_q, spec.s_q, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = stream.cuda_stream
+    d = op.dims
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        smla.sparse_mla_sched_meta(d, num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+        if ev is not None:
+            ev[1].record(stream)
+        smla.sparse_mla_decode_fwd(d, num_sms, wl.q.data_ptr(), wl.kv.data_ptr(),
+                                   wl.indices.data_ptr(), wl.sm_scale, op.sched.data_ptr(),
+                                   op.workspace.data_ptr(), op.accum_bytes, out.data_ptr(),
+                                   lse.data_ptr(), st)
+        if ev is not None:
+            ev[2].record(stream)
+        smla.sparse_mla_combine(d, num_sms, op.sched.data_ptr(), op.workspace.data_ptr(),
+                                op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    if op.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if op.device_status() != 0:
+        raise RuntimeError("device status word set during the timed steps")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    sched_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    comb_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = sum(step_ms) / len(step_ms) / 1e3
+    t_dec = sum(dec_ms) / len(dec_ms) / 1e3
+    if ws > 1:
+        tt = torch.tensor([t_step, t_dec], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step, t_dec = tt.tolist()
+
+    flops = workloads.flops_valid(wl)
+    flops_all = 2.0 * spec.h_q * (576 + 512) * spec.b * spec.s_q * spec.topk
+    nvalid = wl.num_valid
+    alg_bytes = workloads.alg_bytes(wl)
+    value = ws * flops / t_step / 1e12
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / t_dec / 1e12
+    traffic = traffic_from_profiles(
+        os.path.join(ROOT, "sparse_mla_attention_decode_gb300", "csrc", "decode_fwd.cu"), spec.name)
+
+    # ---- end to end through the public API with host buffers (KV cache resident)
+    q_h = wl.q.cpu().pin_memory()
+    i_h = wl.indices.cpu().pin_memory()
+    o_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    l_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(wl.q)
+    i_d = torch.empty_like(wl.indices)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        i_d.copy_(i_h, non_blocking=True)
+        op.run(q_d, wl.kv, i_d, wl.sm_scale, out=out, lse=lse)
+        o_h.copy_(out, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_times = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e_times.append(time.perf_counter() - t1)
+    t_e2e = sum(e_times) / len(e_times)
+    h2d = q_h.numel() * q_h.element_size() + i_h.numel() * i_h.element_size()
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        r = time_oracle(wl, args.cpu_budget)
+        cpu = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s",
+               "cores": r["threads"], "kind": "oracle",
+               "sample": f"first {r['tokens']} of {spec.b * spec.s_q} query tokens of "
+                         f"{spec.name}, all heads ({r['seconds']:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
+                       "topk": spec.topk, "ctx": spec.ctx, "num_blocks": int(wl.kv.shape[0]),
+                       "valid_slots": nvalid, "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
+                       "l2": "flushed between steps (256 MiB write, outside the step time)"},
+            "gathered_tokens_per_s": ws * nvalid / t_step,
+            "tflops_all_slots": ws * flops_all / t_step / 1e12,
+            "kernel_ms": {"sched_meta": statistics.mean(sched_ms),
+                          "decode": statistics.mean(dec_ms), "combine": statistics.mean(comb_ms)},
+            "wall_s_timed_region": wall,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} bf16 burst",
+                         "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
+                         "alg_bytes_per_launch": alg_bytes,
+                         "hbm_frac_alg_bytes": alg_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"])},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * flops / t_e2e / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "q and indices host->device, out and lse device->host each step; "
+                            "the KV cache stays resident"},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,168 @@
+/*
+ * sparse_mla.h -- C ABI of libsparse_mla.so: sparse MLA decode attention over a paged FP8
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("FlashMLA 与 DSA：内核、流水线和正确性边界", section 4.3, and "FlashMLA
+ * Sparse Decode 完整计算过程详解", steps 1-19): for every query token t = (batch bi,
+ * position si) and query head h,
+ *
+ *     J      = the top-k slots j of token t whose index is a valid physical token id
+ *     K_j    = decoded 576-dim key of cache row indices[t][j] (512 dequantized NoPE dims,
+ *              64 bf16 RoPE dims);  V_j = K_j[0:512]
+ *     s_j    = sm_scale * <q[t][h], K_j>
+ *     lse    = ln sum_{j in J} exp(s_j)
+ *     out    = sum_{j in J} exp(s_j - lse) V_j
+ *
+ * with out = 0 and lse = +inf when J is empty.  MLA decodes as MQA: all h_q heads share
+ * one latent KV head (h_kv = 1).
+ *
+ * Work is split in three calls, all asynchronous on the caller's CUDA stream:
+ *   1. sparse_mla_sched_meta  -- greedy split-KV partition plan, computed on the GPU
+ *   2. sparse_mla_decode_fwd  -- gather + dequant + QK^T + online softmax + PV
+ *   3. sparse_mla_combine     -- LSE-weighted merge of the split partial results
+ *
+ * Conventions shared by every entry point:
+ *   - All buffers are owned by the caller.  The library allocates no memory, keeps no
+ *     global state and never synchronises a stream, except sparse_mla_read_device_status.
+ *   - Pointers marked "device" must be device-accessible memory on the current device.
+ *   - Arguments are validated before anything is launched; a bad argument returns an error
+ *     and launches nothing.  The library never aborts the process and never prints.
+ *   - A failed CUDA launch returns SMLA_ERR_CUDA (cudaGetLastError is read and cleared).
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - The same smla_dims and num_sms must be used for the three calls of one problem.
+ */
+#ifndef SPARSE_MLA_H_
+#define SPARSE_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1, /* null pointer, negative size, size overflow */
+  SMLA_ERR_UNSUPPORTED = 2, /* a shape outside h_q in {64,128}, d_qk = 576, d_v = 512,
+                               page_block_size = 64 */
+  SMLA_ERR_ALIGNMENT = 3,   /* a pointer below its required alignment */
+  SMLA_ERR_WORKSPACE = 4,   /* a caller buffer smaller than sparse_mla_workspace_size says */
+  SMLA_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  SMLA_ERR_TIMEOUT = 6,     /* device status: a bounded wait inside a kernel ran out */
+  SMLA_ERR_DEVICE = 7       /* device status: a kernel reported bad data (see below) */
+} smla_status;
+
+/* Bits of the device status word (sparse_mla_read_device_status). */
+#define SMLA_DEV_TIMEOUT 0x1u       /* a pipeline wait gave up; outputs are not valid */
+#define SMLA_DEV_Q_RANGE 0x2u       /* |q| above 65504: not representable in the fp16 MMA */
+#define SMLA_DEV_SCALE_RANGE 0x4u   /* a KV scale * 256 outside the fp16 normal range */
+
+/* Problem sizes.  Only d_qk = 576, d_v = 512, page_block_size = 64, h_q in {64, 128} are
+ * supported ("FlashMLA 与 DSA", section 3.1: the 656-byte V3.2 row; section 6.1: h_q 64/128,
+ * d_v 512).  topk may be any value >= 0; b or s_q = 0 is an empty problem. */
+typedef struct {
+  int32_t b;               /* batch (requests) */
+  int32_t s_q;             /* query tokens per request */
+  int32_t h_q;             /* query heads: 64 or 128 */
+  int32_t d_qk;            /* 576 = 512 NoPE + 64 RoPE */
+  int32_t d_v;             /* 512 */
+  int32_t topk;            /* index slots per query token */
+  int32_t page_block_size; /* 64 tokens per cache page */
+  int64_t num_blocks;      /* pages in the KV cache pool; num_blocks * 64 <= 2^31 - 1 */
+} smla_dims;
+
+/*
+ * sparse_mla_workspace_size -- sizes of the two caller-owned device buffers.
+ *   num_sms      SMs the plan may use; <= 0 means "all SMs of the current device".
+ *   sched_bytes  out: bytes for the partition plan (sparse_mla_sched_meta writes it).
+ *   accum_bytes  out: bytes for the split-partial workspace (fp32 partial O and base-2 lse
+ *                of at most b + num_sm_parts splits per query position).
+ * Host-only; launches nothing.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED,
+ * SMLA_ERR_CUDA (device query failed).
+ */
+smla_status sparse_mla_workspace_size(const smla_dims* dims, int num_sms, size_t* sched_bytes,
+                                      size_t* accum_bytes);
+
+/*
+ * sparse_mla_sched_meta -- the greedy split-KV plan ("FlashMLA Sparse Decode 完整计算过程
+ * 详解", step 3; "FlashMLA 与 DSA", section 3.2).  One warp on the GPU computes:
+ *   num_sm_parts = max(num_sms / s_q / 2, 1)        (one partition = one pair of SMs)
+ *   blocks per request = ceil(topk / 64), overhead 5 per request,
+ *   payload = ceil(sum(blocks + 5) / num_sm_parts) + 5,
+ * then fills partitions left to right, splitting a request where it does not fit.
+ *   sched_meta   device, 16-byte aligned, sched_bytes long (caller-owned, written here):
+ *                int32 [num_sm_parts][8] {begin_req, end_req, begin_block, end_block
+ *                (exclusive), begin_split_idx, is_first_req_splitted,
+ *                is_last_req_splitted, 0}, then int32 num_splits prefix [b + 1], then the
+ *                device status word (reset to 0 by this call).
+ * Asynchronous on stream.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED,
+ * SMLA_ERR_ALIGNMENT, SMLA_ERR_WORKSPACE, SMLA_ERR_CUDA.
+ */
+smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sched_meta,
+                                  size_t sched_bytes, void* stream);
+
+/*
+ * sparse_mla_decode_fwd -- the split-KV attention pass ("FlashMLA Sparse Decode 完整计算过程
+ * 详解", steps 5-15).  Each partition is run by a cluster of two CTAs; CTA r owns NoPE dims
+ * [256 r, 256 r + 256) and RoPE dims [32 r, 32 r + 32), forms its partial scores with
+ * tcgen05 MMAs, the pair adds the two partials through distributed shared memory, and
+ * each CTA accumulates its half of O.
+ *   q          device bf16 [b][s_q][h_q][576], contiguous, 16-byte aligned
+ *   kv_cache   device uint8 [num_blocks][64][1][656], contiguous, 16-byte aligned; row =
+ *              512 e4m3 NoPE codes | 4 fp32 scales (dequant multipliers, one per 128 dims)
+ *              | 64 bf16 RoPE values
+ *   indices    device int32 [b][s_q][topk], contiguous, 8-byte aligned; value = physical
+ *              token id page * 64 + offset; a value outside [0, num_blocks * 64) (for
+ *              example -1) masks the slot; a repeated id counts once per slot
+ *   sm_scale   softmax scale applied to q.K (for example 1/sqrt(576))
+ *   sched_meta device, the plan written by sparse_mla_sched_meta for the same dims/num_sms
+ *   workspace  device, >= accum_bytes, 16-byte aligned: split partials (read by combine)
+ *   out        device bf16 [b][s_q][h_q][512], 16-byte aligned; rows of unsplit requests
+ *              are final after this call, split rows after sparse_mla_combine
+ *   lse        device fp32 [b][h_q][s_q] (note the axis order), natural log, +inf for a
+ *              row with no valid slot
+ * Asynchronous on stream.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED,
+ * SMLA_ERR_ALIGNMENT, SMLA_ERR_WORKSPACE, SMLA_ERR_CUDA.  Device-side problems (a wait
+ * that ran out, q or a scale outside the fp16 range) set bits of the status word.
+ */
+smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void* q,
+                                  const void* kv_cache, const int32_t* indices, float sm_scale,
+                                  const void* sched_meta, void* workspace,
+                                  size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/*
+ * sparse_mla_combine -- merge split partials ("FlashMLA Sparse Decode 完整计算过程详解",
+ * step 16; "FlashMLA 与 DSA", section 3.2): per (token, head) with n > 1 splits,
+ * M = max_j lse2_j, w_j = 2^(lse2_j - M), out = sum_j w_j o_j / sum_j w_j (bf16),
+ * lse = (M + log2 sum_j w_j) ln 2; all splits empty gives out = 0, lse = +inf.  Rows of
+ * unsplit requests are left untouched.
+ *   sched_meta, workspace   as passed to sparse_mla_decode_fwd (read only)
+ *   out, lse                as for sparse_mla_decode_fwd (written for split rows)
+ * Asynchronous on stream; must follow sparse_mla_decode_fwd on the same stream.
+ * Errors: as sparse_mla_decode_fwd.
+ */
+smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* sched_meta,
+                               const void* workspace, size_t workspace_bytes, void* out,
+                               float* lse, void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* sparse_mla_status_string(smla_status status);
+
+/*
+ * sparse_mla_read_device_status -- copy the device status word out of sched_meta into
+ * *code (SMLA_DEV_* bits, 0 = clean).  Synchronises stream (the only call that does).
+ * Returns SMLA_ERR_TIMEOUT if the TIMEOUT bit is set, SMLA_ERR_DEVICE for other bits,
+ * SMLA_OK when clean; SMLA_ERR_INVALID_ARG / SMLA_ERR_CUDA on bad input or a CUDA error.
+ */
+smla_status sparse_mla_read_device_status(const smla_dims* dims, int num_sms,
+                                          const void* sched_meta, int* code, void* stream);
+
+/* Library build identifier (static storage). */
+const char* sparse_mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H_ */

@@ -1,0 +1,197 @@
+"""Sparse MLA decode attention for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over ``libsparse_mla.so`` (C ABI in ``include/sparse_mla.h``): the
+functions below carry the same names as the C entry points and only marshal arguments.
+Every step of the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and calling into the library without the built extension raises.
+
+PyTorch is used for device memory and streams only (``SparseMLADecode`` allocates the
+caller-owned plan, workspace and outputs as torch tensors).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "SMLA_OK", "SparseMLAError", "smla_dims", "lib", "build", "library_path",
+    "sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
+    "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
+    "sparse_mla_version", "SparseMLADecode", "dims_for",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsparse_mla.so")
+_lock = threading.Lock()
+_lib = None
+
+SMLA_OK = 0
+SMLA_ERR_TIMEOUT = 6
+SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
+EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
+            "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
+            "sparse_mla_version"]
+
+
+class SparseMLAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {sparse_mla_status_string(code)} (status {code})")
+
+
+class smla_dims(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int32), ("s_q", ctypes.c_int32), ("h_q", ctypes.c_int32),
+                ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("page_block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it first (sparse_mla_attention_decode_gb300."
+                    "build() or __graft_entry__.build()); there is no fallback path")
+            L = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.POINTER
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            L.sparse_mla_workspace_size.argtypes = [P(smla_dims), ctypes.c_int, P(sz), P(sz)]
+            L.sparse_mla_sched_meta.argtypes = [P(smla_dims), ctypes.c_int, vp, sz, vp]
+            L.sparse_mla_decode_fwd.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, vp,
+                                                ctypes.c_float, vp, vp, sz, vp, vp, vp]
+            L.sparse_mla_combine.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, sz, vp, vp, vp]
+            L.sparse_mla_status_string.argtypes = [ctypes.c_int]
+            L.sparse_mla_status_string.restype = ctypes.c_char_p
+            L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
+                                                        P(ctypes.c_int), vp]
+            L.sparse_mla_version.restype = ctypes.c_char_p
+            for f in EXPORTED:
+                if f not in ("sparse_mla_status_string", "sparse_mla_version"):
+                    getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != SMLA_OK:
+        raise SparseMLAError(rc, where)
+
+
+def sparse_mla_status_string(code: int) -> str:
+    return lib().sparse_mla_status_string(int(code)).decode()
+
+
+def sparse_mla_version() -> str:
+    return lib().sparse_mla_version().decode()
+
+
+def sparse_mla_workspace_size(dims: smla_dims, num_sms: int = 0) -> tuple[int, int]:
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().sparse_mla_workspace_size(ctypes.byref(dims), int(num_sms), ctypes.byref(a),
+                                           ctypes.byref(b)), "sparse_mla_workspace_size")
+    return a.value, b.value
+
+
+def sparse_mla_sched_meta(dims: smla_dims, num_sms: int, sched_meta: int, sched_bytes: int,
+                          stream: int = 0) -> None:
+    _check(lib().sparse_mla_sched_meta(ctypes.byref(dims), int(num_sms), sched_meta,
+                                       int(sched_bytes), stream), "sparse_mla_sched_meta")
+
+
+def sparse_mla_decode_fwd(dims: smla_dims, num_sms: int, q: int, kv_cache: int, indices: int,
+                          sm_scale: float, sched_meta: int, workspace: int, workspace_bytes: int,
+                          out: int, lse: int, stream: int = 0) -> None:
+    _check(lib().sparse_mla_decode_fwd(ctypes.byref(dims), int(num_sms), q, kv_cache, indices,
+                                       float(sm_scale), sched_meta, workspace,
+                                       int(workspace_bytes), out, lse, stream),
+           "sparse_mla_decode_fwd")
+
+
+def sparse_mla_combine(dims: smla_dims, num_sms: int, sched_meta: int, workspace: int,
+                       workspace_bytes: int, out: int, lse: int, stream: int = 0) -> None:
+    _check(lib().sparse_mla_combine(ctypes.byref(dims), int(num_sms), sched_meta, workspace,
+                                    int(workspace_bytes), out, lse, stream),
+           "sparse_mla_combine")
+
+
+def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int,
+                                  stream: int = 0) -> tuple[int, int]:
+    """(status code of the call, device status word)."""
+    code = ctypes.c_int()
+    rc = lib().sparse_mla_read_device_status(ctypes.byref(dims), int(num_sms), sched_meta,
+                                             ctypes.byref(code), stream)
+    return rc, code.value
+
+
+def dims_for(b: int, s_q: int, h_q: int, topk: int, num_blocks: int) -> smla_dims:
+    return smla_dims(b, s_q, h_q, 576, 512, topk, 64, num_blocks)
+
+
+class SparseMLADecode:
+    """Owns the plan and workspace buffers of one problem shape and runs the three calls.
+
+    q: bf16 [b, s_q, h_q, 576]; kv_cache: uint8 [num_blocks, 64, 1, 656]; indices: int32
+    [b, s_q, topk]; returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, h_q, s_q]).
+    """
+
+    def __init__(self, b: int, s_q: int, h_q: int, topk: int, num_blocks: int, device=None,
+                 num_sms: int = 0):
+        import torch
+        self.device = torch.device(device if device is not None else "cuda")
+        if num_sms <= 0:
+            num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.num_sms = int(num_sms)
+        self.dims = dims_for(b, s_q, h_q, topk, num_blocks)
+        sb, ab = sparse_mla_workspace_size(self.dims, self.num_sms)
+        self.sched_bytes, self.accum_bytes = sb, ab
+        self.sched = torch.empty(max(sb, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.empty(max(ab, 16), dtype=torch.uint8, device=self.device)
+
+    def run(self, q, kv_cache, indices, sm_scale: float, out=None, lse=None, stream=None):
+        import torch
+        d = self.dims
+        if out is None:
+            out = torch.empty(d.b, d.s_q, d.h_q, 512, dtype=torch.bfloat16, device=self.device)
+        if lse is None:
+            lse = torch.empty(d.b, d.h_q, d.s_q, dtype=torch.float32, device=self.device)
+        st = (stream if stream is not None else torch.cuda.current_stream(self.device)).cuda_stream
+        for name, t in (("q", q), ("kv_cache", kv_cache), ("indices", indices), ("out", out),
+                        ("lse", lse)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        sparse_mla_sched_meta(d, self.num_sms, self.sched.data_ptr(), self.sched_bytes, st)
+        sparse_mla_decode_fwd(d, self.num_sms, q.data_ptr(), kv_cache.data_ptr(),
+                              indices.data_ptr(), sm_scale, self.sched.data_ptr(),
+                              self.workspace.data_ptr(), self.accum_bytes, out.data_ptr(),
+                              lse.data_ptr(), st)
+        sparse_mla_combine(d, self.num_sms, self.sched.data_ptr(), self.workspace.data_ptr(),
+                           self.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+        return out, lse
+
+    def device_status(self, stream=None) -> int:
+        import torch
+        st = (stream if stream is not None else torch.cuda.current_stream(self.device)).cuda_stream
+        rc, word = sparse_mla_read_device_status(self.dims, self.num_sms, self.sched.data_ptr(), st)
+        return word
+
+    def plan(self):
+        """(meta int32 [parts, 8], num_splits prefix int32 [b + 1]) copied to the host."""
+        parts = max(self.num_sms // max(self.dims.s_q, 1) // 2, 1)
+        raw = self.sched.cpu()
+        meta = raw[: parts * 32].view(dtype=__import__("torch").int32).view(parts, 8)
+        pre = raw[parts * 32: parts * 32 + (self.dims.b + 1) * 4].view(
+            dtype=__import__("torch").int32)
+        return meta, pre

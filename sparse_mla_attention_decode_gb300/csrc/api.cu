@@ -1,0 +1,192 @@
+// Host runtime of libsparse_mla.so: argument validation, buffer sizing and kernel launches
+// behind the C ABI declared in include/sparse_mla.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/sparse_mla.h"
+#include "smla_internal.h"
+
+using namespace smla;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+smla_status check_dims(const smla_dims* d) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->b < 0 || d->s_q < 0 || d->topk < 0 || d->num_blocks < 0) return SMLA_ERR_INVALID_ARG;
+  if (d->h_q != 64 && d->h_q != 128) return SMLA_ERR_UNSUPPORTED;
+  if (d->d_qk != kDQk || d->d_v != kDV || d->page_block_size != kPage) return SMLA_ERR_UNSUPPORTED;
+  if (d->num_blocks * static_cast<int64_t>(kPage) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
+  const int64_t tokens = static_cast<int64_t>(d->b) * d->s_q;
+  if (tokens > INT32_MAX / 128 || static_cast<int64_t>(d->topk) * tokens > (int64_t(1) << 40))
+    return SMLA_ERR_UNSUPPORTED;
+  if (d->s_q > 65535) return SMLA_ERR_UNSUPPORTED;  // grid.y
+  return SMLA_OK;
+}
+
+smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+  }
+  const int sq = d->s_q > 0 ? d->s_q : 1;
+  int p = num_sms / sq / 2;
+  *parts = p < 1 ? 1 : p;
+  return SMLA_OK;
+}
+
+smla_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SMLA_OK;
+  (void)cudaGetLastError();
+  return SMLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sparse_mla_version(void) { return "sparse_mla 0.1 sm_103a"; }
+
+const char* sparse_mla_status_string(smla_status s) {
+  switch (s) {
+    case SMLA_OK: return "ok";
+    case SMLA_ERR_INVALID_ARG: return "invalid argument";
+    case SMLA_ERR_UNSUPPORTED: return "unsupported shape";
+    case SMLA_ERR_ALIGNMENT: return "misaligned pointer";
+    case SMLA_ERR_WORKSPACE: return "buffer too small";
+    case SMLA_ERR_CUDA: return "CUDA error";
+    case SMLA_ERR_TIMEOUT: return "device wait timed out";
+    case SMLA_ERR_DEVICE: return "device reported bad data";
+  }
+  return "unknown status";
+}
+
+smla_status sparse_mla_workspace_size(const smla_dims* dims, int num_sms, size_t* sched_bytes,
+                                      size_t* accum_bytes) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  if (!sched_bytes || !accum_bytes) return SMLA_ERR_INVALID_ARG;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  *sched_bytes = plan_layout(dims->b, parts).bytes;
+  *accum_bytes = accum_layout(dims->b, dims->s_q, dims->h_q, parts).bytes;
+  return SMLA_OK;
+}
+
+smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sched_meta,
+                                  size_t sched_bytes, void* stream) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  if (!sched_meta) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(sched_meta, 16)) return SMLA_ERR_ALIGNMENT;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  const PlanLayout L = plan_layout(dims->b, parts);
+  if (sched_bytes < L.bytes) return SMLA_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(sched_meta);
+  if (dims->b == 0) {  // empty problem: only the status word needs clearing
+    return cuda_status(cudaMemsetAsync(base + L.status_off, 0, 16, static_cast<cudaStream_t>(stream)));
+  }
+  return cuda_status(launch_sched(dims->b, dims->s_q, dims->topk, parts,
+                                  reinterpret_cast<int32_t*>(base + L.meta_off),
+                                  reinterpret_cast<int32_t*>(base + L.prefix_off),
+                                  reinterpret_cast<uint32_t*>(base + L.status_off),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void* q,
+                                  const void* kv_cache, const int32_t* indices, float sm_scale,
+                                  const void* sched_meta, void* workspace, size_t workspace_bytes,
+                                  void* out, float* lse, void* stream) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
+  if (tokens == 0) return SMLA_OK;
+  if (!q || !sched_meta || !out || !lse || !workspace) return SMLA_ERR_INVALID_ARG;
+  if (dims->topk > 0 && (!indices || (dims->num_blocks > 0 && !kv_cache))) return SMLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 16) ||
+      !aligned(sched_meta, 16) || !aligned(indices, 4) || !aligned(lse, 4))
+    return SMLA_ERR_ALIGNMENT;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
+  if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->topk == 0)
+    return cuda_status(launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse,
+                                         tokens * dims->h_q, tokens * dims->h_q, s));
+  const PlanLayout L = plan_layout(dims->b, parts);
+  const uint8_t* plan = static_cast<const uint8_t*>(sched_meta);
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kv = static_cast<const uint8_t*>(kv_cache);
+  p.indices = indices;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.o_accum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.o_off);
+  p.lse_accum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.lse_off);
+  p.meta = reinterpret_cast<const int32_t*>(plan + L.meta_off);
+  p.nsplits = reinterpret_cast<const int32_t*>(plan + L.prefix_off);
+  p.status = const_cast<uint32_t*>(reinterpret_cast<const uint32_t*>(plan + L.status_off));
+  p.b = dims->b;
+  p.s_q = dims->s_q;
+  p.h_q = dims->h_q;
+  p.topk = dims->topk;
+  p.num_rows = static_cast<int>(dims->num_blocks * kPage);
+  p.score_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 / 256.0);
+  return cuda_status(launch_decode(p, parts, s));
+}
+
+smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* sched_meta,
+                               const void* workspace, size_t workspace_bytes, void* out, float* lse,
+                               void* stream) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
+  if (tokens == 0 || dims->topk == 0) return SMLA_OK;
+  if (!sched_meta || !workspace || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(workspace, 16) || !aligned(sched_meta, 16) || !aligned(lse, 4))
+    return SMLA_ERR_ALIGNMENT;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
+  if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
+  const PlanLayout L = plan_layout(dims->b, parts);
+  CombineParams p;
+  p.o_accum = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + A.o_off);
+  p.lse_accum = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + A.lse_off);
+  p.nsplits = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(sched_meta) + L.prefix_off);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.b = dims->b;
+  p.s_q = dims->s_q;
+  p.h_q = dims->h_q;
+  return cuda_status(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status sparse_mla_read_device_status(const smla_dims* dims, int num_sms,
+                                          const void* sched_meta, int* code, void* stream) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  if (!sched_meta || !code) return SMLA_ERR_INVALID_ARG;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  const PlanLayout L = plan_layout(dims->b, parts);
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, static_cast<const uint8_t*>(sched_meta) + L.status_off, 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  *code = static_cast<int>(word);
+  if (word & SMLA_DEV_TIMEOUT) return SMLA_ERR_TIMEOUT;
+  if (word) return SMLA_ERR_DEVICE;
+  return SMLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Internal declarations shared by the host runtime and the kernels of libsparse_mla.so.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace smla {
+
+constexpr int kDQk = 576, kDNope = 512, kDRope = 64, kDV = 512;
+constexpr int kRowBytes = 656;  // 512 e4m3 + 4 x fp32 scale + 64 x bf16
+constexpr int kPage = 64;
+constexpr int kTopkBlock = 64;  // slots of the top-k list per pipeline block
+constexpr int kFixedOverhead = 5;
+constexpr int kMetaInts = 8;    // int32 fields per partition in the plan
+
+// Layout of the caller's plan buffer.
+struct PlanLayout {
+  int parts;
+  size_t meta_off, prefix_off, status_off, bytes;
+};
+inline PlanLayout plan_layout(int b, int parts) {
+  PlanLayout L;
+  L.parts = parts;
+  L.meta_off = 0;
+  L.prefix_off = static_cast<size_t>(parts) * kMetaInts * 4;
+  size_t end = L.prefix_off + static_cast<size_t>(b + 1) * 4;
+  L.status_off = (end + 15) & ~static_cast<size_t>(15);
+  L.bytes = L.status_off + 64;
+  return L;
+}
+// Layout of the split-partial workspace: o_accum fp32 [max_splits][s_q][h_q][512] then
+// lse_accum fp32 [max_splits][s_q][h_q] (base-2 log-sum-exp).
+struct AccumLayout {
+  int max_splits;
+  size_t o_off, lse_off, bytes;
+};
+inline AccumLayout accum_layout(int b, int s_q, int h_q, int parts) {
+  AccumLayout L;
+  L.max_splits = b + parts;
+  L.o_off = 0;
+  size_t o_bytes = static_cast<size_t>(L.max_splits) * s_q * h_q * kDV * 4;
+  L.lse_off = (o_bytes + 255) & ~static_cast<size_t>(255);
+  L.bytes = L.lse_off + static_cast<size_t>(L.max_splits) * s_q * h_q * 4;
+  return L;
+}
+
+struct DecodeParams {
+  const __nv_bfloat16* q;   // [b][s_q][h_q][576]
+  const uint8_t* kv;        // [num_rows][656]
+  const int32_t* indices;   // [b][s_q][topk]
+  __nv_bfloat16* out;       // [b][s_q][h_q][512]
+  float* lse;               // [b][h_q][s_q]
+  float* o_accum;           // [max_splits][s_q][h_q][512]
+  float* lse_accum;         // [max_splits][s_q][h_q]
+  const int32_t* meta;      // [parts][8]
+  const int32_t* nsplits;   // [b + 1]
+  uint32_t* status;         // device status word
+  int b, s_q, h_q, topk;
+  int num_rows;             // num_blocks * 64
+  float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
+};
+
+struct CombineParams {
+  const float* o_accum;
+  const float* lse_accum;
+  const int32_t* nsplits;
+  __nv_bfloat16* out;
+  float* lse;
+  int b, s_q, h_q;
+};
+
+// Kernel launchers (return the launch's cudaError_t).
+cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int32_t* prefix,
+                         uint32_t* status, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, int64_t rows_o, int64_t n_lse,
+                              cudaStream_t stream);
+
+}  // namespace smla

@@ -1,0 +1,89 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and compare with the
+oracle.  Tolerances come from the accuracy target of this project: O max-abs <= 2e-2,
+relative L2 <= 5e-3 over the compared tensor, LSE abs <= 1e-3 with +inf matching +inf."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import sparse_mla_attention_decode_gb300 as smla
+import workloads
+
+O_MAX_ABS = 2e-2
+O_REL_L2 = 5e-3
+LSE_ABS = 1e-3
+
+
+def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True):
+    dev = wl.q.device
+    op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
+                              wl.kv.shape[0], device=dev, num_sms=num_sms)
+    out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale)
+    torch.cuda.synchronize(dev)
+    if check_status:
+        word = op.device_status()
+        assert word == 0, f"device status word {word:#x}"
+    return out, lse, op
+
+
+def compact_inputs(wl: workloads.Workload, tokens: np.ndarray):
+    """Oracle inputs restricted to ``tokens``: the rows those tokens select are gathered (with
+    torch, from the seeded inputs) into a small pool and their indices renumbered.  Invalid
+    slots stay invalid."""
+    b, s_q = wl.spec.b, wl.spec.s_q
+    nrows = wl.kv.shape[0] * 64
+    idx = wl.indices.view(b * s_q, -1)[torch.as_tensor(tokens, device=wl.indices.device)]
+    valid = (idx >= 0) & (idx < nrows)
+    used = torch.unique(idx[valid])
+    remap = torch.full((nrows,), -1, dtype=torch.int64, device=idx.device)
+    remap[used] = torch.arange(used.numel(), device=idx.device)
+    new_idx = torch.where(valid, remap[idx.clamp(0, nrows - 1).long()], torch.full_like(idx, -1).long())
+    npages = (used.numel() + 63) // 64
+    pool = torch.zeros(max(npages, 1) * 64, 656, dtype=torch.uint8, device=idx.device)
+    pool[: used.numel()] = wl.kv.view(nrows, 656)[used]
+    q = wl.q.view(b * s_q, wl.spec.h_q, 576)[torch.as_tensor(tokens, device=wl.q.device)]
+    n = len(tokens)
+    qb = q.cpu().contiguous().view(torch.int16).numpy().view("uint16").reshape(n, 1, wl.spec.h_q, 576)
+    kvn = pool.cpu().numpy().reshape(-1, 64, 656)
+    idn = new_idx.to(torch.int32).cpu().numpy().reshape(n, 1, -1)
+    return qb, kvn, idn
+
+
+def oracle_tokens(wl: workloads.Workload, tokens, threads: int = 0):
+    """Oracle (out [n, h, 512], lse [n, h]) for the given flattened query tokens."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    qb, kvn, idn = compact_inputs(wl, tokens)
+    out, lse, _ = oracle.sparse_mla_decode(qb, kvn, idn, wl.sm_scale, threads=threads)
+    return out, lse
+
+
+def gpu_tokens(out: torch.Tensor, lse: torch.Tensor, wl: workloads.Workload, tokens):
+    b, s_q, h = wl.spec.b, wl.spec.s_q, wl.spec.h_q
+    t = torch.as_tensor(np.asarray(tokens), device=out.device)
+    o = out.view(b * s_q, h, 512)[t].double().cpu().numpy()
+    l = lse.permute(0, 2, 1).reshape(b * s_q, h)[t].double().cpu().numpy()
+    return o, l
+
+
+def compare(o_gpu, l_gpu, o_ref, l_ref, what: str = ""):
+    """Assert the tolerances; returns the metrics."""
+    assert o_gpu.shape == o_ref.shape and l_gpu.shape == l_ref.shape
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
+    inf_ref = np.isposinf(l_ref)
+    assert np.array_equal(np.isposinf(l_gpu), inf_ref), f"{what}: +inf lse mismatch"
+    assert np.all(np.isfinite(l_gpu[~inf_ref])), f"{what}: non-finite lse"
+    err = np.abs(o_gpu - o_ref)
+    max_abs = float(err.max()) if err.size else 0.0
+    denom = float(np.linalg.norm(o_ref))
+    rel = float(np.linalg.norm(o_gpu - o_ref) / denom) if denom > 0 else float(np.linalg.norm(o_gpu))
+    rows = np.linalg.norm(o_gpu - o_ref, axis=-1) / np.maximum(np.linalg.norm(o_ref, axis=-1), 1e-30)
+    worst_row = float(rows[np.linalg.norm(o_ref, axis=-1) > 0].max()) if np.any(
+        np.linalg.norm(o_ref, axis=-1) > 0) else 0.0
+    lse_err = float(np.abs(l_gpu[~inf_ref] - l_ref[~inf_ref]).max()) if np.any(~inf_ref) else 0.0
+    assert np.all(o_gpu[inf_ref] == 0.0), f"{what}: all-masked rows must be 0"
+    assert max_abs <= O_MAX_ABS, f"{what}: max abs {max_abs}"
+    assert rel <= O_REL_L2, f"{what}: rel L2 {rel}"
+    assert lse_err <= LSE_ABS, f"{what}: lse abs {lse_err}"
+    return {"max_abs": max_abs, "rel_l2": rel, "worst_row_rel": worst_row, "lse_abs": lse_err}

@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports every entry point its header declares, and rejects bad
+arguments before launching anything (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mla_attention_decode_gb300 as smla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    smla.build()
+    return smla.lib()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(sparse_mla_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert {"sparse_mla_sched_meta", "sparse_mla_decode_fwd", "sparse_mla_combine"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(smla.EXPORTED) == names
+
+
+def test_status_strings(L):
+    assert smla.sparse_mla_status_string(0) == "ok"
+    assert "unsupported" in smla.sparse_mla_status_string(2)
+    assert smla.sparse_mla_status_string(99) == "unknown status"
+    assert "sm_103a" in smla.sparse_mla_version()
+
+
+def test_workspace_sizes(L):
+    d = smla.dims_for(64, 1, 128, 2048, 32768)
+    sb, ab = smla.sparse_mla_workspace_size(d, 152)
+    parts = 152 // 1 // 2
+    assert sb >= parts * 32 + 65 * 4 + 4
+    assert ab >= (64 + parts) * 128 * 512 * 4 + (64 + parts) * 128 * 4
+
+
+@pytest.mark.parametrize("field,value,code", [("h_q", 96, 2), ("d_qk", 512, 2), ("d_v", 256, 2),
+                                              ("page_block_size", 32, 2), ("b", -1, 1),
+                                              ("topk", -5, 1), ("num_blocks", 1 << 26, 2)])
+def test_bad_dims_rejected(L, field, value, code):
+    d = smla.dims_for(2, 1, 128, 128, 64)
+    setattr(d, field, value)
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.sparse_mla_workspace_size(ctypes.byref(d), 152, ctypes.byref(a), ctypes.byref(b)) == code
+
+
+def test_pointer_checks_before_launch(L):
+    d = smla.dims_for(2, 1, 128, 128, 64)
+    sb, ab = smla.sparse_mla_workspace_size(d, 152)
+    fake = 0x10000
+    # null plan
+    assert L.sparse_mla_sched_meta(ctypes.byref(d), 152, None, sb, None) == 1
+    # misaligned plan
+    assert L.sparse_mla_sched_meta(ctypes.byref(d), 152, fake + 4, sb, None) == 3
+    # plan buffer too small
+    assert L.sparse_mla_sched_meta(ctypes.byref(d), 152, fake, sb - 1, None) == 4
+    args = dict(q=fake, kv=fake, idx=fake, plan=fake, ws=fake, out=fake, lse=fake)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return L.sparse_mla_decode_fwd(ctypes.byref(d), 152, a["q"], a["kv"], a["idx"],
+                                       ctypes.c_float(0.0417), a["plan"], a["ws"],
+                                       kw.get("wsb", ab), a["out"], a["lse"], None)
+
+    assert call(q=None) == 1
+    assert call(out=fake + 8) == 3
+    assert call(kv=fake + 8) == 3
+    assert call(wsb=ab - 1) == 4
+    assert L.sparse_mla_decode_fwd(ctypes.byref(d), 152, fake, fake, fake, ctypes.c_float(float("nan")),
+                                   fake, fake, ab, fake, fake, None) == 1
+    assert L.sparse_mla_combine(ctypes.byref(d), 152, fake, fake, ab - 1, fake, fake, None) == 4
+    code = ctypes.c_int()
+    assert L.sparse_mla_read_device_status(ctypes.byref(d), 152, None, ctypes.byref(code), None) == 1
+
+
+def test_no_device_is_a_cuda_error_not_a_crash(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    d = smla.dims_for(2, 1, 128, 128, 64)
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    # num_sms <= 0 asks the library to query the device: on a machine without one -> CUDA error
+    assert L.sparse_mla_workspace_size(ctypes.byref(d), 0, ctypes.byref(a), ctypes.byref(b)) == 5
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The package and its kernels never import, link or read anything under oracle/."""
+    pkg = os.path.join(ROOT, "sparse_mla_attention_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "oracle" not in txt.lower(), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            txt = open(os.path.join(ROOT, "oracle", f), encoding="utf-8").read()
+            assert "sparse_mla_attention_decode_gb300" not in txt and "sparse_mla.h" not in txt, f

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on seeded inputs.
+
+Small cases are compared in full (several pipeline blocks, split and unsplit requests, ragged
+top-k tails, masked / out-of-range / duplicate slots, all-masked rows, h_q = 64 and 128,
+fp32 and power-of-two scales).  The five benchmark workloads run at their full sizes in the
+launch configuration the benchmark uses, and sampled query tokens are compared with the
+oracle computed for those tokens."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle import sched as osched
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import sparse_mla_attention_decode_gb300 as smla
+    smla.lib()  # the library must load; there is no fallback
+    return torch.device("cuda:0")
+
+
+def _full(wl, num_sms, what):
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms)
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    ro, rl = oracle.sparse_mla_decode_full(q, kv, idx, wl.sm_scale)
+    go = out.double().cpu().numpy()
+    gl = lse.double().cpu().numpy()
+    return gu.compare(go.reshape(-1, wl.spec.h_q, 512), gl.transpose(0, 2, 1).reshape(-1, wl.spec.h_q),
+                      ro.reshape(-1, wl.spec.h_q, 512), rl.transpose(0, 2, 1).reshape(-1, wl.spec.h_q), what)
+
+
+# ----------------------------------------------------------------------------- planner
+
+@pytest.mark.parametrize("b,s_q,topk,num_sms", [(2, 1, 128, 132), (64, 1, 2048, 152),
+                                                (32, 1, 2048, 152), (128, 2, 2048, 152),
+                                                (1, 4096, 2048, 152), (3, 1, 100, 14),
+                                                (7, 3, 1000, 40), (200, 1, 64, 6)])
+def test_sched_meta_matches_oracle(dev, b, s_q, topk, num_sms):
+    import sparse_mla_attention_decode_gb300 as smla
+    op = smla.SparseMLADecode(b, s_q, 128, topk, 16, device=dev, num_sms=num_sms)
+    smla.sparse_mla_sched_meta(op.dims, num_sms, op.sched.data_ptr(), op.sched_bytes,
+                               torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    meta, pre = op.plan()
+    parts = osched.num_sm_parts(num_sms, s_q)
+    plan, prefix = osched.plan([topk] * b, parts)
+    assert pre.tolist() == prefix
+    for p_ref, row in zip(plan, meta.tolist()):
+        if p_ref.empty(b):
+            assert row[0] >= b
+            continue
+        assert row[:7] == [p_ref.begin_req, p_ref.end_req, p_ref.begin_block, p_ref.end_block,
+                           p_ref.begin_split_idx, int(p_ref.is_first_req_splitted),
+                           int(p_ref.is_last_req_splitted)]
+
+
+# ----------------------------------------------------------------------------- small, full compare
+
+SMALL = [
+    # (name, kwargs, num_sms) -- num_sms controls how many partitions (and so splits) exist
+    ("b2_h128_k128_nosplit", dict(b=2, h_q=128, topk=128, ctx=1024), 8),
+    ("b2_h128_k128_split", dict(b=2, h_q=128, topk=128, ctx=1024), 132),
+    ("b3_h128_k300_ragged_masked", dict(b=3, h_q=128, topk=300, ctx=2048, masked_per_row=37), 40),
+    ("b2_sq2_h64_k256_causal", dict(b=2, s_q=2, h_q=64, topk=256, ctx=1024, causal_base=700), 24),
+    ("b4_h128_k512_ue8m0_sorted", dict(b=4, h_q=128, topk=512, ctx=4096, ue8m0=True,
+                                       sort_indices=True), 20),
+    ("b1_h128_k2048_many_splits", dict(b=1, h_q=128, topk=2048, ctx=8192), 152),
+    ("b5_h64_k64_oneblock", dict(b=5, h_q=64, topk=64, ctx=512, masked_per_row=10), 152),
+    ("b2_h128_k17_tiny", dict(b=2, h_q=128, topk=17, ctx=256), 4),
+]
+
+
+@pytest.mark.parametrize("name,kw,num_sms", SMALL, ids=[s[0] for s in SMALL])
+def test_small_parity(dev, name, kw, num_sms):
+    wl = workloads.small(device=dev, seed=hash(name) % 1000, **kw)
+    m = _full(wl, num_sms, name)
+    print(name, m)
+
+
+def test_all_masked_out_of_range_and_duplicates(dev):
+    wl = workloads.small(b=4, h_q=128, topk=192, ctx=1024, device=dev, seed=9)
+    nrows = wl.kv.shape[0] * 64
+    idx = wl.indices.clone()
+    idx[1] = -1                                   # a request with no valid slot at all
+    idx[2, 0, :64] = -1                           # a whole leading block masked
+    idx[2, 0, 100:110] = nrows + 5                # out of range counts as masked
+    idx[2, 0, 110:115] = -123456
+    idx[3, 0, 1:40] = idx[3, 0, 0]                # duplicates count once per slot
+    wl.indices = idx.contiguous()
+    for num_sms in (4, 64):                       # unsplit and split plans
+        m = _full(wl, num_sms, f"edge_{num_sms}")
+        print(m)
+
+
+def test_topk_zero_and_empty(dev):
+    import sparse_mla_attention_decode_gb300 as smla
+    wl = workloads.small(b=2, h_q=64, topk=4, ctx=256, device=dev)
+    op = smla.SparseMLADecode(2, 1, 64, 0, wl.kv.shape[0], device=dev)
+    out, lse = op.run(wl.q, wl.kv, wl.indices[:, :, :0].contiguous(), wl.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isposinf(lse))
+    op0 = smla.SparseMLADecode(0, 1, 128, 64, 4, device=dev)
+    o0, l0 = op0.run(wl.q[:0], wl.kv, wl.indices[:0], wl.sm_scale)
+    assert o0.numel() == 0 and l0.numel() == 0
+
+
+def test_combine_kernel_vs_oracle(dev):
+    """The combine kernel alone on synthetic split partials (including empty splits)."""
+    import sparse_mla_attention_decode_gb300 as smla
+    from oracle import combine as ocomb
+    b, s_q, h = 3, 2, 64
+    op = smla.SparseMLADecode(b, s_q, h, 2048, 64, device=dev, num_sms=40)
+    st = torch.cuda.current_stream().cuda_stream
+    smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+    torch.cuda.synchronize()
+    meta, pre = op.plan()
+    pre = pre.tolist()
+    parts = max(op.num_sms // s_q // 2, 1)
+    max_splits = b + parts
+    g = torch.Generator(device="cpu").manual_seed(4)
+    o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)
+    l_acc = torch.randn(max_splits, s_q, h, generator=g) * 4
+    l_acc[pre[0], 0, :5] = -math.inf                      # some empty splits
+    l_acc[pre[1]:pre[2], 1, 7] = -math.inf                # a row whose splits are all empty
+    o_off = 0
+    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
+    wsb = op.workspace
+    wsb[o_off:o_off + o_acc.numel() * 4].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
+    wsb[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
+    out = torch.full((b, s_q, h, 512), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((b, h, s_q), 7.0, dtype=torch.float32, device=dev)
+    smla.sparse_mla_combine(op.dims, op.num_sms, op.sched.data_ptr(), wsb.data_ptr(),
+                            op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+    torch.cuda.synchronize()
+    out, lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    for r in range(b):
+        n = pre[r + 1] - pre[r]
+        for s in range(s_q):
+            for hh in range(h):
+                if n <= 1:
+                    assert np.all(out[r, s, hh] == 7.0) and lse[r, hh, s] == 7.0
+                    continue
+                ro, rl = ocomb.combine(l_acc[pre[r]:pre[r + 1], s, hh].double().numpy(),
+                                       o_acc[pre[r]:pre[r + 1], s, hh].double().numpy())
+                if math.isinf(rl):
+                    assert np.all(out[r, s, hh] == 0) and np.isposinf(lse[r, hh, s])
+                else:
+                    assert np.max(np.abs(out[r, s, hh] - ro)) <= 1e-2 * max(1, np.abs(ro).max())
+                    assert abs(lse[r, hh, s] - rl) <= 1e-4
+
+
+def test_split_partials_match_oracle(dev):
+    """Split-KV partials written by the decode pass equal the oracle on each split's slots."""
+    wl = workloads.small(b=2, h_q=128, topk=256, ctx=2048, masked_per_row=11, device=dev, seed=21)
+    out, lse, op = gu.run_cuda(wl, num_sms=24)
+    meta, pre = op.plan()
+    parts = max(op.num_sms // 1 // 2, 1)
+    plan, prefix = osched.plan([256] * 2, parts)
+    assert pre.tolist() == prefix
+    max_splits = 2 + parts
+    ws = op.workspace.cpu()
+    o_acc = ws[: max_splits * 128 * 512 * 4].view(torch.float32).view(max_splits, 1, 128, 512)
+    lse_off = ((max_splits * 128 * 512 * 4) + 255) // 256 * 256
+    l_acc = ws[lse_off: lse_off + max_splits * 128 * 4].view(torch.float32).view(max_splits, 1, 128)
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    checked = 0
+    for p in plan:
+        if p.empty(2):
+            continue
+        for r in range(p.begin_req, p.end_req + 1):
+            if prefix[r + 1] - prefix[r] == 1:
+                continue
+            lo, hi = osched.block_range(p, r, 4)
+            slot = p.begin_split_idx if r == p.begin_req else prefix[r]
+            ro, rl, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, tokens=[r],
+                                                 slot_range=(lo * 64, hi * 64))
+            go = o_acc[slot, 0].double().numpy()
+            gl = l_acc[slot, 0].double().numpy() / oracle.online.LOG2E  # base 2 -> natural
+            gu.compare(go[None], gl[None], ro, rl, f"split {slot}")
+            checked += 1
+    assert checked >= 2
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+def _sample_tokens(n_tok, k, seed):
+    rng = np.random.default_rng(seed)
+    pick = set([0, n_tok - 1])
+    while len(pick) < min(k, n_tok):
+        pick.add(int(rng.integers(0, n_tok)))
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("cfg", list(workloads.CONFIGS))
+def test_benchmark_workload_parity(dev, cfg):
+    spec = workloads.CONFIGS[cfg]
+    wl = workloads.make(spec, device=dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms)
+    n_tok = spec.b * spec.s_q
+    # properties at any size: finite outputs, finite lse on rows with a valid slot
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
+    tokens = _sample_tokens(n_tok, 24 if n_tok > 24 else n_tok, spec.seed)
+    ro, rl = gu.oracle_tokens(wl, tokens)
+    go, gl = gu.gpu_tokens(out, lse, wl, tokens)
+    m = gu.compare(go, gl, ro, rl, cfg)
+    print(cfg, m)
