@@ -18,9 +18,8 @@
 //     O in all 512 tensor-memory columns) and writes the normalised output.
 //
 // Data moves between the two SMs in one direction only (17 KB per 64-slot block), and P is
-// exactly the fp16 matrix the MMA uses, so the split adds no rounding.  Gathers are warp loads
-// (16 bytes per thread, one block of look-ahead in registers); a prefetch warp pulls every row
-// of a request range into L2 when the range starts.
+// exactly the fp16 matrix the MMA uses, so the split adds no rounding.  Rows are gathered with
+// cp.async straight into shared memory, one block of rows ahead of the conversion.
 //
 // Keys and values are dequantized as 256 * K (folded back into the score scale and into the
 // final 1/L) so that small fp32 scales stay in the fp16 normal range.  Invalid slots become NaN
@@ -46,13 +45,16 @@ constexpr int MSG_ALPHA = P_BYTES;      // 128 x fp32 rescale factors
 constexpr int MSG_INVL = P_BYTES + 512; // 128 x fp32 1 / (256 L) (last block of a range)
 constexpr int MSG_BYTES = P_BYTES + 1024;
 constexpr int MSG_STRIDE = 18432;       // 1024-aligned message slots
-constexpr int NSTAGE = 2;               // tile / message double buffering
+constexpr int NSTAGE = 2;               // tile double buffering
+constexpr int NMSG = 2;                 // message slots (S-CTA staging = O-CTA receive)
 constexpr int NSBUF = 3;                // score buffers in tensor memory (S-CTA)
+constexpr int RAW_BYTES = 8 * 8 * 656;  // gathered-row rings of the 8 dequant warps (S-CTA size)
 
 constexpr int OFF_TILE = 0;                                  // KT[2] or VT[2]
 constexpr int OFF_MSG = NSTAGE * KT_STAGE;                   // S: staging, O: receive
-constexpr int OFF_MISC = OFF_MSG + NSTAGE * MSG_STRIDE;
-static_assert(OFF_MSG % 1024 == 0 && OFF_MISC % 1024 == 0, "alignment");
+constexpr int OFF_RAW = OFF_MSG + NMSG * MSG_STRIDE;         // gathered rows
+constexpr int OFF_MISC = OFF_RAW + RAW_BYTES;
+static_assert(OFF_MSG % 1024 == 0 && OFF_RAW % 1024 == 0 && OFF_MISC % 16 == 0, "alignment");
 
 enum Bar {
   // S-CTA
@@ -61,17 +63,17 @@ enum Bar {
   B_S_FULL = B_KT_EMPTY + 2,        // [3] commit after QK
   B_S_EMPTY = B_S_FULL + NSBUF,     // [3] 128 softmax threads
   B_Q_FULL = B_S_EMPTY + NSBUF,     // 128 softmax threads
-  B_MSG_FREE = B_Q_FULL + 1,        // [2] remote arrival from the O-CTA after PV consumed it
+  B_MSG_FREE = B_Q_FULL + 1,        // [3] remote arrival from the O-CTA after PV consumed it
   // O-CTA
-  B_VT_FULL = B_MSG_FREE + 2,       // [2] 256 dequant threads
+  B_VT_FULL = B_MSG_FREE + NMSG,    // [2] 256 dequant threads
   B_VT_EMPTY = B_VT_FULL + 2,       // [2] commit after PV
-  B_MSG_FULL = B_VT_EMPTY + 2,      // [2] 1 local expect-tx arrival + the bulk copy's bytes
-  B_CORR = B_MSG_FULL + 2,          // [2] 128 correction threads
-  B_PV_DONE = B_CORR + 2,           // [2] commit after PV
-  B_O_FULL = B_PV_DONE + 2,         // commit after the last PV of a range
+  B_MSG_FULL = B_VT_EMPTY + 2,      // [3] 1 local expect-tx arrival + the bulk copy's bytes
+  B_CORR = B_MSG_FULL + NMSG,       // [3] 128 correction threads
+  B_PV_DONE = B_CORR + NMSG,        // [3] commit after PV
+  B_O_FULL = B_PV_DONE + NMSG,      // commit after the last PV of a range
   B_O_EMPTY = B_O_FULL + 1,         // 128 epilogue threads
   B_DRAIN = B_O_EMPTY + 1,          // MMA drain on the way out
-  B_STAGED = B_DRAIN + 1,           // [2] 128 softmax threads wrote a message slot (S-CTA)
+  B_STAGED = B_DRAIN + 1,           // [3] 128 softmax threads wrote a message slot (S-CTA)
   NUM_BARS
 };
 constexpr int OFF_BARS = OFF_MISC;
@@ -82,7 +84,7 @@ constexpr int SMEM_BYTES = OFF_STARTED + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // warps: 0-3 softmax (S) / correction + epilogue (O); 4-11 gather + dequant; 12 MMA;
-// 13 L2 prefetch (S) / message relay (O)
+// 13 message relay (O; idle on the S-CTA).
 constexpr int NTHREADS = 448;
 constexpr uint32_t TM_Q = 0, TM_S = 288;  // S-CTA columns; the O-CTA uses all 512 for O
 constexpr uint32_t IDESC_QK = umma_idesc_f16(128, BT, 0);
@@ -111,7 +113,7 @@ struct Ctx {
     uint64_t deadline = 0;
     for (uint32_t i = 0;; ++i) {
       if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-      if ((i & 127u) == 127u) {
+      if ((i & 7u) == 7u) {
         if (*abort_flag) return false;
         const uint64_t now = globaltimer_ns();
         if (deadline == 0) {
@@ -165,123 +167,167 @@ struct Cursor {
 };
 
 // ---------------------------------------------------------------------------------------
-// Gather + dequant (warps 4-11 of both CTAs).  Thread t owns row t % 64 of every block and
-// the 128-dim scale group q = t / 64 of its NoPE part (plus RoPE dims [16 q, 16 q + 16) on the
-// S-CTA).  The loads of block g + 1 are issued before block g is converted.
-struct RowData {
-  uint4 nope[8];
-  uint4 rope[2];
-  uint4 scales;
-  bool valid;
+// Gather + dequant (warps 4-11 of both CTAs).  Warp w owns rows w, w + 8, ..., w + 56 of every
+// block and handles them four at a time: the eight lanes 8 r .. 8 r + 7 share a row, and lane
+// j of the eight copies and converts 16-byte code chunks j, j + 8, j + 16, j + 24 of it
+// (dims [16 c, 16 c + 16) of chunk c) and, on the S-CTA, RoPE chunk j; lane 0 of the eight
+// also copies the 4 scales.  Rows are copied global -> shared with cp.async into a per-warp
+// ring of 8 row slots that runs one block ahead of the conversion, so a block of rows per
+// warp is in flight and no row passes through registers before it has landed.  A slot whose
+// index is masked is zero-filled without a read.
+constexpr int RING = 8;  // row slots per dequant warp
+template <bool kScores>
+struct RowCopy {
+  static constexpr int kBytes = kScores ? kRowBytes : kDNope + 16;  // 656 or 528 bytes per slot
 };
+static_assert(8 * RING * RowCopy<true>::kBytes <= RAW_BYTES, "row ring");
 
 __device__ __forceinline__ int32_t load_index(const DecodeParams& p, int s, int req, int blk,
                                               int row) {
   const int slot = blk * BT + row;
   if (slot >= p.topk) return -1;
-  return __ldg(p.indices + (static_cast<size_t>(req) * p.s_q + s) * p.topk + slot);
+  return ldg_s32(p.indices + (static_cast<size_t>(req) * p.s_q + s) * p.topk + slot);
 }
 
+// Copies this lane's share of one row (j = lane % 8) into its ring slot; one commit group per
+// call covers the four rows of the warp step.
 template <bool kScores>
-__device__ __forceinline__ void load_row(const DecodeParams& p, int32_t idx, int q, RowData& d) {
-  d.valid = idx >= 0 && idx < p.num_rows;
-  if (!d.valid) return;
-  const uint4* row = reinterpret_cast<const uint4*>(p.kv + static_cast<size_t>(idx) * kRowBytes);
+__device__ __forceinline__ void issue_rows(const DecodeParams& p, int32_t idx, uint32_t slot,
+                                           int j) {
+  const bool ok = idx >= 0 && idx < p.num_rows;
+  const uint8_t* src = p.kv + static_cast<size_t>(ok ? idx : 0) * kRowBytes;
+  const uint32_t n = ok ? 16u : 0u;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) d.nope[k] = __ldg(row + q * 8 + k);
-  d.scales = __ldg(row + 32);
-  if (kScores) {
-    d.rope[0] = __ldg(row + 33 + q * 2);
-    d.rope[1] = __ldg(row + 34 + q * 2);
-  }
+  for (int k = 0; k < 4; ++k) cp_async16(slot + (j + 8 * k) * 16, src + (j + 8 * k) * 16, n);
+  if (j == 0) cp_async16(slot + kDNope, src + kDNope, n);  // scales
+  if (kScores) cp_async16(slot + kDNope + 16 + j * 16, src + kDNope + 16 + j * 16, n);  // RoPE
+  cp_async_commit();
 }
 
+// Converts this lane's share of one landed row into the fp16 tile (row `row`).
 template <bool kScores>
-__device__ __forceinline__ void store_row(uint32_t tile, int row, int q, const RowData& d,
-                                          uint32_t& bad) {
-  const uint32_t c0 = tile + (2 * q) * CHUNK;  // chunks 2q, 2q + 1 hold dims [128 q, 128 q + 128)
-  if (d.valid) {
-    const uint32_t sel =
-        q == 0 ? d.scales.x : q == 1 ? d.scales.y : q == 2 ? d.scales.z : d.scales.w;
-    const float scale = __uint_as_float(sel) * 256.f;
-    bad |= !(scale >= 6.103515625e-05f && scale <= 65504.f);
-    const uint32_t s2 = pack_f16x2(scale, scale);
+__device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool valid,
+                                           const uint4 (&nope)[4], const uint4& scales,
+                                           const uint4& rope, uint32_t& bad) {
+  // code chunk c = j + 8 k -> 64-dim tile chunk c / 4 = j / 4 + 2 k, 8-dim sub-chunks
+  // 2 (j % 4) and + 1; lanes 4-7 of the eight store their odd sub-chunk first, so the eight
+  // lanes of a row hit 8 distinct 16-byte bank groups with every store (no bank conflict)
+  const uint32_t flip = (j >> 2) & 1;
+  const uint32_t u0 = 2 * (j & 3) + flip, u1 = 2 * (j & 3) + (flip ^ 1u);
+  const uint32_t ch0 = tile + (j >> 2) * CHUNK;
+  if (valid) {
+    const uint32_t sc[4] = {scales.x, scales.y, scales.z, scales.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t w[4] = {d.nope[k].x, d.nope[k].y, d.nope[k].z, d.nope[k].w};
+    for (int k = 0; k < 4; ++k) {  // code chunk j + 8 k lies in scale group k
+      const float scale = __uint_as_float(sc[k]) * 256.f;
+      bad |= !(scale >= 6.103515625e-05f && scale <= 65504.f);
+      const uint32_t sc2 = pack_f16x2(scale, scale);
+      const uint32_t w[4] = {nope[k].x, nope[k].y, nope[k].z, nope[k].w};
       uint32_t o[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        o[2 * e] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[e] & 0xFFFFu)), s2);
-        o[2 * e + 1] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[e] >> 16)), s2);
+        o[2 * e] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[e] & 0xFFFFu)), sc2);
+        o[2 * e + 1] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[e] >> 16)), sc2);
       }
-      // 16 codes = dims [128 q + 16 k, + 16): chunk 2q + k / 4, 8-dim chunks 2 (k % 4) and + 1
-      const uint32_t ch = c0 + (k >> 2) * CHUNK;
-      st_shared_v4(ch + sw128_chunk(row, 2 * (k & 3)), o[0], o[1], o[2], o[3]);
-      st_shared_v4(ch + sw128_chunk(row, 2 * (k & 3) + 1), o[4], o[5], o[6], o[7]);
+      const uint32_t ch = ch0 + 2 * k * CHUNK;
+      st_shared_v4(ch + sw128_chunk(row, u0), flip ? o[4] : o[0], flip ? o[5] : o[1],
+                   flip ? o[6] : o[2], flip ? o[7] : o[3]);
+      st_shared_v4(ch + sw128_chunk(row, u1), flip ? o[0] : o[4], flip ? o[1] : o[5],
+                   flip ? o[2] : o[6], flip ? o[3] : o[7]);
     }
     if (kScores) {
+      const uint32_t r[4] = {rope.x, rope.y, rope.z, rope.w};
+      uint32_t q[4];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint32_t w[4] = {d.rope[k].x, d.rope[k].y, d.rope[k].z, d.rope[k].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * 256.f,
-                            __uint_as_float(w[e] & 0xFFFF0000u) * 256.f);
-        st_shared_v4(tile + 8 * CHUNK + sw128_chunk(row, 2 * q + k), o[0], o[1], o[2], o[3]);
-      }
+      for (int e = 0; e < 4; ++e)
+        q[e] = pack_f16x2(__uint_as_float(r[e] << 16) * 256.f,
+                          __uint_as_float(r[e] & 0xFFFF0000u) * 256.f);
+      st_shared_v4(tile + 8 * CHUNK + sw128_chunk(row, j), q[0], q[1], q[2], q[3]);
     }
   } else {
     // invalid slot: NaN key (its score becomes NaN and is masked) or zero value
     const uint32_t f = kScores ? F16_NAN2 : 0u;
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      st_shared_v4(c0 + (k >> 3) * CHUNK + sw128_chunk(row, k & 7), f, f, f, f);
-    if (kScores) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        st_shared_v4(tile + 8 * CHUNK + sw128_chunk(row, 2 * q + k), f, f, f, f);
+    for (int k = 0; k < 4; ++k) {
+      st_shared_v4(ch0 + 2 * k * CHUNK + sw128_chunk(row, u0), f, f, f, f);
+      st_shared_v4(ch0 + 2 * k * CHUNK + sw128_chunk(row, u1), f, f, f, f);
     }
+    if (kScores) st_shared_v4(tile + 8 * CHUNK + sw128_chunk(row, j), f, f, f, f);
   }
 }
 
 template <bool kScores>
 __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int s, int t) {
-  const int row = t & 63, q = t >> 6;
+  using RC = RowCopy<kScores>;
+  const int w = t >> 5, lane = t & 31;  // warp w of the 8 dequant warps
+  const int j = lane & 7, rsel = lane >> 3;
   const int bfull = kScores ? B_KT_FULL : B_VT_FULL;
   const int bempty = kScores ? B_KT_EMPTY : B_VT_EMPTY;
   const int stage_bytes = kScores ? KT_STAGE : VT_STAGE;
+  const uint32_t ring = c.sbase + OFF_RAW + w * RING * RC::kBytes;
   uint32_t bad = 0;
-  Cursor cur, ahead;
+  // Lane r < 8 holds the index of row w + 8 r of a block.
+  auto idx_of = [&](const Cursor& k) -> int32_t {
+    return (lane < 8 && !k.done(pl)) ? load_index(p, s, k.req, k.blk, w + 8 * lane) : -1;
+  };
+  auto valid_bits = [&](int32_t ix) -> uint32_t {
+    return __ballot_sync(0xffffffffu, lane < 8 && ix >= 0 && ix < p.num_rows) & 0xFFu;
+  };
+  Cursor cur, fetch;
   cur.start(pl);
-  ahead = cur;
-  RowData d[2];
-  load_row<kScores>(p, load_index(p, s, cur.req, cur.blk, row), q, d[0]);
-  ahead.next(pl);
-  int32_t idx_next = ahead.done(pl) ? -1 : load_index(p, s, ahead.req, ahead.blk, row);
+  fetch = cur;
+  // prologue: the first block's rows in flight, the second block's indices loaded
+  const int32_t ix0 = idx_of(fetch);
+  uint32_t vmask = valid_bits(ix0);  // bits 8 k + r: row r of block cur + k is valid
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = 4 * h + rsel;
+    issue_rows<kScores>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j);
+  }
+  fetch.next(pl);
+  int32_t ixA = idx_of(fetch);  // block cur + 1
+  fetch.next(pl);
   uint32_t g = 0;
 #pragma unroll 1
   while (!cur.done(pl)) {
+    const uint32_t st = g & 1;
+    Cursor ah = cur;
+    ah.next(pl);
+    const bool issue_more = !ah.done(pl);  // block cur + 1 exists
+    const int32_t ixB = idx_of(fetch);      // block cur + 2, loaded one block early
+    vmask |= valid_bits(ixA) << 8;
+    if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
+    {
+      const uint32_t tile = c.sbase + OFF_TILE + st * stage_bytes;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int r = 4 * h + rsel;  // this lane's row of the block: w + 8 r
+        cp_async_wait<1>();          // the copies of this step (the older group) have landed
+        __syncwarp();
+        const uint32_t slot = ring + r * RC::kBytes;
+        uint4 nope[4], scales, rope = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {  // unrolled by two so the row buffers stay in registers
-      if (cur.done(pl)) break;
-      // look-ahead: issue the loads of the next block before converting this one
-      if (!ahead.done(pl)) {
-        load_row<kScores>(p, idx_next, q, d[u ^ 1]);
-        ahead.next(pl);
-        idx_next = ahead.done(pl) ? -1 : load_index(p, s, ahead.req, ahead.blk, row);
+        for (int k = 0; k < 4; ++k)
+          ld_shared_v4(slot + (j + 8 * k) * 16, nope[k].x, nope[k].y, nope[k].z, nope[k].w);
+        ld_shared_v4(slot + kDNope, scales.x, scales.y, scales.z, scales.w);
+        if (kScores) ld_shared_v4(slot + kDNope + 16 + j * 16, rope.x, rope.y, rope.z, rope.w);
+        __syncwarp();  // every lane has read the slot: it can take the next block's row
+        const int32_t nx = __shfl_sync(0xffffffffu, ixA, r);
+        if (issue_more) issue_rows<kScores>(p, nx, slot, j);
+        else cp_async_commit();  // an empty group keeps the count per step uniform
+        store_rows<kScores>(tile, w + 8 * r, j, (vmask >> r) & 1u, nope, scales, rope, bad);
       }
-      const uint32_t st = g & 1;
-      if (g >= NSTAGE && !c.wait(bempty + st, ((g >> 1) - 1) & 1)) goto out;
-      store_row<kScores>(c.sbase + OFF_TILE + st * stage_bytes, row, q, d[u], bad);
-      fence_proxy_async_smem();
-      mbar_arrive(c.bar(bfull + st));
-      cur.next(pl);
-      ++g;
     }
+    fence_proxy_async_smem();
+    mbar_arrive(c.bar(bfull + st));
+    vmask >>= 8;
+    ixA = ixB;
+    fetch.next(pl);
+    cur.next(pl);
+    ++g;
   }
 out:
+  cp_async_wait<0>();  // no copy may land after the CTA has moved on
   if (bad) atomicOr(c.status, SMLA_DEV_SCALE_RANGE);
 }
 
@@ -296,12 +342,12 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase) {
       if (!c.wait(B_KT_FULL + st, (g >> 1) & 1)) return;
       if (g >= NSBUF && !c.wait(B_S_EMPTY + sb, ((g / NSBUF) - 1) & 1)) return;
       tc_fence_after();
-      const uint32_t kt = c.sbase + OFF_TILE + st * KT_STAGE;
+      const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * KT_STAGE, 16, 1024, 2);
       const uint32_t d = tbase + TM_S + sb * BT;
 #pragma unroll
-      for (int kk = 0; kk < 36; ++kk)
-        mma_ts(d, tbase + TM_Q + kk * 8,
-               umma_desc(kt + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024, 2), IDESC_QK, kk > 0);
+      for (int kk = 0; kk < 36; ++kk)  // descriptor start addresses advance in 16-byte units
+        mma_ts(d, tbase + TM_Q + kk * 8, bdesc + ((((kk >> 2) * CHUNK) + (kk & 3) * 32) >> 4),
+               IDESC_QK, kk > 0);
       mma_commit(c.bar(B_S_FULL + sb));
       mma_commit(c.bar(B_KT_EMPTY + st));
     }
@@ -314,25 +360,24 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     for (int blk = b0; blk < b1; ++blk, ++g) {
-      const uint32_t st = g & 1, par = (g >> 1) & 1;
+      const uint32_t st = g & 1, ms = g % NMSG, mpar = (g / NMSG) & 1;
       const bool first = blk == b0;
-      if (!c.wait(B_VT_FULL + st, par)) return;
-      if (!c.wait(B_MSG_FULL + st, par, true)) return;
-      if (!c.wait(B_CORR + st, par)) return;
+      if (!c.wait(B_VT_FULL + st, (g >> 1) & 1)) return;
+      if (!c.wait(B_MSG_FULL + ms, mpar, true)) return;
+      if (!c.wait(B_CORR + ms, mpar)) return;
       if (first && item >= 1 && !c.wait(B_O_EMPTY, (item - 1) & 1)) return;
       tc_fence_after();
-      const uint32_t pm = c.sbase + OFF_MSG + st * MSG_STRIDE;
-      const uint32_t vt = c.sbase + OFF_TILE + st * VT_STAGE;
+      const uint64_t adesc = umma_desc(c.sbase + OFF_MSG + ms * MSG_STRIDE, 16, 1024, 2);
+      const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * VT_STAGE, CHUNK, 1024, 2);
 #pragma unroll
       for (int kk = 0; kk < BT / 16; ++kk) {
-        const uint64_t a = umma_desc(pm + kk * 32, 16, 1024, 2);
 #pragma unroll
-        for (int nh = 0; nh < 2; ++nh)
-          mma_ss(tbase + nh * 256, a, umma_desc(vt + nh * 4 * CHUNK + kk * 2048, CHUNK, 1024, 2),
-                 IDESC_PV, !(first && kk == 0));
+        for (int nh = 0; nh < 2; ++nh)  // descriptor start addresses advance in 16-byte units
+          mma_ss(tbase + nh * 256, adesc + (kk * 32 >> 4),
+                 bdesc + ((nh * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV, !(first && kk == 0));
       }
       mma_commit(c.bar(B_VT_EMPTY + st));
-      mma_commit(c.bar(B_PV_DONE + st));
+      mma_commit(c.bar(B_PV_DONE + ms));
       if (blk == b1 - 1) mma_commit(c.bar(B_O_FULL));
     }
   }
@@ -346,21 +391,31 @@ __device__ void stage_q(const DecodeParams& p, const Ctx& c, uint32_t tq, int to
   const uint4* src = reinterpret_cast<const uint4*>(
       p.q + (static_cast<size_t>(tok) * p.h_q + (live ? i : 0)) * kDQk);
 #pragma unroll 1
-  for (int cc = 0; cc < 18; ++cc) {  // 18 x 32 dims
-    uint32_t w[16];
+  for (int batch = 0; batch < 3; ++batch) {  // 3 x 192 dims: all loads of a batch in flight
+    uint4 v[24];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 v = live ? __ldg(src + cc * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    for (int k = 0; k < 24; ++k)
+      v[k] = ldg_v4(src + batch * 24 + k);  // rows past h_q read head 0 and are zeroed below
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t r = pack_f16x2(__uint_as_float(in[e] << 16),
-                                      __uint_as_float(in[e] & 0xFFFF0000u));
-        bad |= ((r & 0x7C00u) == 0x7C00u) | ((r & 0x7C000000u) == 0x7C000000u);
-        w[4 * k + e] = r;
+    for (int cc = 0; cc < 6; ++cc) {  // 6 x 32 dims = 6 x 16 columns
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t in[4] = {v[cc * 4 + k].x, v[cc * 4 + k].y, v[cc * 4 + k].z, v[cc * 4 + k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t r = pack_f16x2(__uint_as_float(in[e] << 16),
+                                        __uint_as_float(in[e] & 0xFFFF0000u));
+          bad |= ((r & 0x7C00u) == 0x7C00u) | ((r & 0x7C000000u) == 0x7C000000u);
+          w[4 * k + e] = r;
+        }
       }
+      if (!live) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = 0u;
     }
-    tmem_st16(tq + cc * 16, w);
+    tmem_st16(tq + (batch * 6 + cc) * 16, w);
+    }
   }
   tmem_wait_st();
   tc_fence_before();
@@ -387,7 +442,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
     float m = -INFINITY;  // running max (base-2 units) used as the exponent reference
     float l = 0.f;        // running exp-sum against m
     for (int blk = b0; blk < b1; ++blk, ++g) {
-      const uint32_t sb = g % NSBUF, st = g & 1;
+      const uint32_t sb = g % NSBUF, st = g % NMSG;
       if (!c.wait_warp(B_S_FULL + sb, (g / NSBUF) & 1)) goto out;
       tc_fence_after();
       uint32_t sr[BT];
@@ -416,7 +471,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       }
       const float mref = m == -INFINITY ? 0.f : m;
       // the message slot is free again once the O-CTA's PV that read it has finished
-      if (g >= NSTAGE && !c.wait_warp(B_MSG_FREE + st, ((g >> 1) - 1) & 1, true)) goto out;
+      if (g >= NMSG && !c.wait_warp(B_MSG_FREE + st, ((g / NMSG) - 1) & 1, true)) goto out;
       const uint32_t msg = c.sbase + OFF_MSG + st * MSG_STRIDE;
       float sum = 0.f;
 #pragma unroll
@@ -452,7 +507,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       fence_proxy_async_smem();
       mbar_arrive(c.bar(B_STAGED + st));
       if (i == 0) {  // all 128 rows are in the slot: ship it to the O-CTA
-        if (!c.wait(B_STAGED + st, (g >> 1) & 1)) goto out;
+        if (!c.wait(B_STAGED + st, (g / NMSG) & 1)) goto out;
         bulk_s2s_cluster(peer_msg + st * MSG_STRIDE, msg, MSG_BYTES, peer_full + st * 8);
       }
     }
@@ -461,32 +516,6 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   }
 out:
   if (qbad) atomicOr(c.status, SMLA_DEV_Q_RANGE);
-}
-
-// S-CTA prefetch warp: when a request range starts, pull every selected row into L2.
-__device__ void role_prefetch(const DecodeParams& p, const Ctx& c, const Plan& pl, int s,
-                              int lane) {
-  volatile uint32_t* started = reinterpret_cast<volatile uint32_t*>(
-      __cvta_shared_to_generic(c.sbase + OFF_STARTED));
-  uint32_t item = 0;
-  for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
-    // run one request range ahead of the softmax (prefetches are hints: give up quietly)
-    const uint64_t deadline = globaltimer_ns() + kWaitNs;
-    while (*started < item && !*c.abort_flag && globaltimer_ns() < deadline) {
-    }
-    if (*c.abort_flag) return;
-    const int32_t* idx = p.indices + (static_cast<size_t>(req) * p.s_q + s) * p.topk;
-    const int lo = pl.first_block(req) * BT;
-    const int hi = min(pl.last_block(req) * BT, p.topk);
-    for (int j = lo + lane; j < hi; j += 32) {
-      const int32_t id = __ldg(idx + j);
-      if (id < 0 || id >= p.num_rows) continue;
-      const uint8_t* row = p.kv + static_cast<size_t>(id) * kRowBytes;
-#pragma unroll
-      for (int k = 0; k < 6; ++k) prefetch_l2(row + k * 128);
-      prefetch_l2(row + kRowBytes - 1);
-    }
-  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -500,15 +529,15 @@ __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const 
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     float invl = 0.f;
     for (int blk = b0; blk < b1; ++blk, ++g) {
-      const uint32_t st = g & 1;
+      const uint32_t st = g % NMSG;
       if (i == 0) mbar_arrive_expect_tx(c.bar(B_MSG_FULL + st), MSG_BYTES);
-      if (!c.wait_warp(B_MSG_FULL + st, (g >> 1) & 1, true)) return;
+      if (!c.wait_warp(B_MSG_FULL + st, (g / NMSG) & 1, true)) return;
       const uint32_t msg = c.sbase + OFF_MSG + st * MSG_STRIDE;
       const float alpha = ld_shared_f32(msg + MSG_ALPHA + 4 * i);
       if (blk == b1 - 1) invl = ld_shared_f32(msg + MSG_INVL + 4 * i);
       if (blk > b0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         // the S-CTA moved this row's reference: rescale O once the previous PV has landed
-        if (!c.wait_warp(B_PV_DONE + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+        if (!c.wait_warp(B_PV_DONE + ((g - 1) % NMSG), ((g - 1) / NMSG) & 1)) return;
         tc_fence_after();
 #pragma unroll 1
         for (int k = 0; k < 512; k += 16) {
@@ -581,8 +610,8 @@ __device__ void role_relay(const Ctx& c, const Plan& pl) {
   uint32_t g = 0;
   for (int req = pl.begin_req; req <= pl.end_req; ++req)
     for (int blk = pl.first_block(req); blk < pl.last_block(req); ++blk, ++g) {
-      const uint32_t st = g & 1;
-      if (!c.wait(B_PV_DONE + st, (g >> 1) & 1)) return;
+      const uint32_t st = g % NMSG;
+      if (!c.wait(B_PV_DONE + st, (g / NMSG) & 1)) return;
       mbar_arrive_remote(peer_free + st * 8);
     }
 }
@@ -613,12 +642,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *c.abort_flag = 0u;
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSTAGE; ++b) {
       mbar_init(c.bar(B_KT_FULL + b), 256);
       mbar_init(c.bar(B_KT_EMPTY + b), 1);
-      mbar_init(c.bar(B_MSG_FREE + b), 1);
       mbar_init(c.bar(B_VT_FULL + b), 256);
       mbar_init(c.bar(B_VT_EMPTY + b), 1);
+    }
+    for (int b = 0; b < NMSG; ++b) {
+      mbar_init(c.bar(B_MSG_FREE + b), 1);
       mbar_init(c.bar(B_MSG_FULL + b), 1);
       mbar_init(c.bar(B_CORR + b), 128);
       mbar_init(c.bar(B_PV_DONE + b), 1);
@@ -662,8 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         c.drain(B_DRAIN, 0);
       }
     } else {
-      if (scores) role_prefetch(p, c, pl, s, lane);
-      else if (lane == 0) role_relay(c, pl);
+      if (!scores && lane == 0) role_relay(c, pl);
     }
   }
   tc_fence_before();
