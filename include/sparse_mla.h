@@ -146,6 +146,40 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
                                const void* workspace, size_t workspace_bytes, void* out,
                                float* lse, void* stream);
 
+/*
+ * sparse_mla_decode_static -- sparse_mla_sched_meta, sparse_mla_decode_fwd and
+ * sparse_mla_combine in one call, on scratch memory owned by the library instead of the
+ * caller.  The pages describe no such call: it exists for callers that cannot provide
+ * device buffers of their own, such as a plain C host program with no device allocator at
+ * hand, or a latency-critical loop that may not call cudaMalloc (which can synchronise the
+ * device) once it is running.
+ *   dims, num_sms, q, kv_cache, indices, sm_scale, out, lse, stream
+ *              as for sparse_mla_decode_fwd
+ * Unlike every other entry point, this one uses library-owned state:
+ *   - The scratch is one static device array of SMLA_STATIC_SCRATCH_BYTES (48 MiB) per
+ *     device, created when the library's CUDA module loads; the call allocates nothing.
+ *     A problem whose plan plus split partials (sparse_mla_workspace_size) exceed it is
+ *     rejected with SMLA_ERR_WORKSPACE before anything is launched.  With num_sms = 152
+ *     that admits, for example, b = 64, s_q = 1, h_q = 128 (37 MB) and b = 128, s_q = 2,
+ *     h_q = 64 (44 MB); use the three-call sequence with caller buffers beyond that.
+ *   - The first call on a device, made with that device current, looks up the array's
+ *     device address (cudaGetSymbolAddress, which may load the CUDA module) and caches it;
+ *     make that first call before any stream capture begins.
+ *   - Every call on a device uses the same scratch, so two calls whose executions overlap
+ *     on the GPU (different streams without an ordering between them, or host threads
+ *     issuing at the same time) corrupt each other's results.  Order them, for example by
+ *     issuing all of them on one stream.
+ *   - The planner zeroes the status words at the start of every call and nothing else in
+ *     the scratch needs an initial value; the device status of the last call cannot be
+ *     read back through sparse_mla_read_device_status (its plan is not caller-visible).
+ * Asynchronous on stream.  Errors: as sparse_mla_decode_fwd, plus SMLA_ERR_WORKSPACE for a
+ * problem above the scratch size and SMLA_ERR_CUDA if the address lookup fails.
+ */
+#define SMLA_STATIC_SCRATCH_BYTES (((size_t)48) << 20)
+smla_status sparse_mla_decode_static(const smla_dims* dims, int num_sms, const void* q,
+                                     const void* kv_cache, const int32_t* indices,
+                                     float sm_scale, void* out, float* lse, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* sparse_mla_status_string(smla_status status);
 

@@ -19,7 +19,8 @@ __all__ = [
     "SMLA_OK", "SparseMLAError", "smla_dims", "lib", "build", "library_path",
     "sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
     "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
-    "sparse_mla_version", "SparseMLADecode", "dims_for",
+    "sparse_mla_version", "sparse_mla_decode_static", "STATIC_SCRATCH_BYTES",
+    "SparseMLADecode", "dims_for",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,11 +29,14 @@ _lock = threading.Lock()
 _lib = None
 
 SMLA_OK = 0
+SMLA_ERR_WORKSPACE = 4
 SMLA_ERR_TIMEOUT = 6
 SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
-            "sparse_mla_version"]
+            "sparse_mla_version", "sparse_mla_decode_static"]
+# Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 48 << 20
 
 
 class SparseMLAError(RuntimeError):
@@ -78,6 +82,8 @@ def lib():
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
                                                         P(ctypes.c_int), vp]
             L.sparse_mla_version.restype = ctypes.c_char_p
+            L.sparse_mla_decode_static.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, vp,
+                                                   ctypes.c_float, vp, vp, vp]
             for f in EXPORTED:
                 if f not in ("sparse_mla_status_string", "sparse_mla_version"):
                     getattr(L, f).restype = ctypes.c_int
@@ -125,6 +131,25 @@ def sparse_mla_combine(dims: smla_dims, num_sms: int, sched_meta: int, workspace
     _check(lib().sparse_mla_combine(ctypes.byref(dims), int(num_sms), sched_meta, workspace,
                                     int(workspace_bytes), out, lse, stream),
            "sparse_mla_combine")
+
+
+def sparse_mla_decode_static(dims: smla_dims, num_sms: int, q: int, kv_cache: int,
+                             indices: int, sm_scale: float, out: int, lse: int,
+                             stream: int = 0) -> None:
+    """Plan + decode + combine on the library's own fixed scratch (no caller buffers).
+
+    For callers that cannot allocate device memory.  Calls on one device share the scratch,
+    so their executions must not overlap; the first call on a device should come before
+    any stream capture.  Problems above STATIC_SCRATCH_BYTES are rejected.
+    """
+    rc = lib().sparse_mla_decode_static(ctypes.byref(dims), int(num_sms), q, kv_cache, indices,
+                                        float(sm_scale), out, lse, stream)
+    if rc == SMLA_ERR_WORKSPACE:
+        sb, ab = sparse_mla_workspace_size(dims, num_sms)
+        need = ((ab + 255) // 256) * 256 + sb
+        raise SparseMLAError(rc, f"sparse_mla_decode_static: the problem needs {need} bytes of "
+                                 f"scratch, the fixed scratch holds {STATIC_SCRATCH_BYTES}")
+    _check(rc, "sparse_mla_decode_static")
 
 
 def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int,
