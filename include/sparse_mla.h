@@ -104,15 +104,15 @@ smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sche
 
 /*
  * sparse_mla_decode_fwd -- the split-KV attention pass ("FlashMLA Sparse Decode 完整计算过程
- * 详解", steps 5-15).  Each partition is run by a cluster of two CTAs; CTA r owns NoPE dims
- * [256 r, 256 r + 256) and RoPE dims [32 r, 32 r + 32), forms its partial scores with
- * tcgen05 MMAs, the pair adds the two partials through distributed shared memory, and
- * each CTA accumulates its half of O.
+ * 详解", steps 5-15).  Each partition of the plan runs on a cluster of two CTAs: one gathers
+ * and dequantizes the selected rows into an fp16 key tile, forms the scores with tcgen05 MMAs
+ * and runs the online softmax; it streams P to the other, which gathers the value rows and
+ * accumulates O = P V in tensor memory and writes it out.
  *   q          device bf16 [b][s_q][h_q][576], contiguous, 16-byte aligned
  *   kv_cache   device uint8 [num_blocks][64][1][656], contiguous, 16-byte aligned; row =
  *              512 e4m3 NoPE codes | 4 fp32 scales (dequant multipliers, one per 128 dims)
  *              | 64 bf16 RoPE values
- *   indices    device int32 [b][s_q][topk], contiguous, 8-byte aligned; value = physical
+ *   indices    device int32 [b][s_q][topk], contiguous, 4-byte aligned; value = physical
  *              token id page * 64 + offset; a value outside [0, num_blocks * 64) (for
  *              example -1) masks the slot; a repeated id counts once per slot
  *   sm_scale   softmax scale applied to q.K (for example 1/sqrt(576))
