@@ -451,15 +451,13 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(c.bar(B_S_EMPTY + sb));
-      // mask (NaN = invalid slot) and scale to base-2 units
-      float mx = -INFINITY;
+      // block max in base-2 units: fmaxf skips the NaN scores of invalid slots, and the scale
+      // is positive, so it applies to the max of the raw scores (four chains for ILP)
+      const float c2 = p.score_scale_log2;
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < BT; ++k) {
-        const float x = __uint_as_float(sr[k]);
-        const float t = x == x ? x * p.score_scale_log2 : -INFINITY;
-        sr[k] = __float_as_uint(t);
-        mx = fmaxf(mx, t);
-      }
+      for (int k = 0; k < BT; ++k) mq[k & 3] = fmaxf(mq[k & 3], __uint_as_float(sr[k]));
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c2;
       // lazy rescale: the reference only moves when a block's max passes it by more than 8
       // (p then stays <= 256, which fp16 holds with full precision)
       float alpha = 1.f;
@@ -473,19 +471,22 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       // the message slot is free again once the O-CTA's PV that read it has finished
       if (g >= NMSG && !c.wait_warp(B_MSG_FREE + st, ((g / NMSG) - 1) & 1, true)) goto out;
       const uint32_t msg = c.sbase + OFF_MSG + st * MSG_STRIDE;
-      float sum = 0.f;
+      // p = 2^(s * c2 - mref); an invalid slot's NaN stays NaN through ex2 and fmaxf(NaN, 0)
+      // turns it into p = 0
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(__uint_as_float(sr[8 * k + 2 * e]) - mref);
-          const float p1 = ex2(__uint_as_float(sr[8 * k + 2 * e + 1]) - mref);
-          sum += p0 + p1;
+          const float p0 = fmaxf(ex2(fmaf(__uint_as_float(sr[8 * k + 2 * e]), c2, -mref)), 0.f);
+          const float p1 = fmaxf(ex2(fmaf(__uint_as_float(sr[8 * k + 2 * e + 1]), c2, -mref)), 0.f);
+          sq[e] += p0 + p1;
           w[e] = pack_f16x2(p0, p1);
         }
         st_shared_v4(msg + sw128_chunk(i, k), w[0], w[1], w[2], w[3]);
       }
+      const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
       l = l * alpha + sum;
       st_shared_f32(msg + MSG_ALPHA + 4 * i, alpha);
       if (blk == b1 - 1) {
@@ -630,16 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   c.abort_flag = reinterpret_cast<volatile uint32_t*>(sm + OFF_ABORT);
   c.status = p.status;
   c.role = 0;
-  const int32_t* m = p.meta + part * kMetaInts;
-  Plan pl;
-  pl.begin_req = m[0];
-  pl.end_req = m[1];
-  pl.begin_block = m[2];
-  pl.end_block = m[3];
-  pl.begin_split = m[4];
-  pl.nb = (p.topk + BT - 1) / BT;
-  const bool active = pl.begin_req < p.b;
 
+  // Set-up that touches no input: it overlaps the tail of the preceding kernel (the planner)
+  // when this launch is allowed to start early.
   if (threadIdx.x == 0) {
     *c.abort_flag = 0u;
     for (int b = 0; b < NSTAGE; ++b) {
@@ -667,7 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     fence_mbar_init_cluster();
   }
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM_SLOT);
-  if (warp == 12 && active) {
+  if (warp == 12) {
     tmem_alloc(c.sbase + OFF_TMEM_SLOT, 512);
     tmem_relinquish();
   }
@@ -675,7 +669,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote access
-  const uint32_t tbase = active ? *tslot : 0u;
+  const uint32_t tbase = *tslot;
+
+  griddep_wait();  // the plan, q, kv and indices of earlier kernels are visible from here on
+  const int32_t* m = p.meta + part * kMetaInts;
+  Plan pl;
+  pl.begin_req = m[0];
+  pl.end_req = m[1];
+  pl.begin_block = m[2];
+  pl.end_block = m[3];
+  pl.begin_split = m[4];
+  pl.nb = (p.topk + BT - 1) / BT;
+  const bool active = pl.begin_req < p.b;
 
   if (active) {
     c.role = (scores ? 0u : 8u) + (warp < 4 ? 1u : warp < 12 ? 2u : warp == 12 ? 3u : 4u);
@@ -699,7 +704,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 12 && active) tmem_dealloc(tbase, 512);
+  if (warp == 12) tmem_dealloc(tbase, 512);
   cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
 }
 
@@ -709,9 +714,19 @@ cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream)
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(2 * parts), static_cast<unsigned>(p.s_q), 1);
-  decode_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the kernel's set-up may overlap the preceding kernel;
+  // griddepcontrol.wait inside holds every read of the plan and the inputs until it is done.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * parts), static_cast<unsigned>(p.s_q), 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, p);
 }
 
 }  // namespace smla

@@ -19,59 +19,106 @@ namespace smla {
 // begin_split_idx, is_first_req_splitted, is_last_req_splitted, 0}, plus the prefix sum of
 // splits per request.  Split slots are numbered in partition order, so the splits of one
 // request are consecutive and prefix[req] is the slot of its first split.
-// The plan is a serial walk over at most b + parts steps, done by one thread.
+//
+// Every request has the same ceil(topk / 64) blocks, so one partition's walk is a few lines of
+// arithmetic: finish the current request if it fits, then as many whole requests as the
+// remaining capacity holds, then split the next one.  Lane 0 walks the partitions in order
+// into shared memory (one thread's global stores would issue one by one); the warp then copies
+// the table out with 16-byte stores and fills the split prefix: a request r has one split
+// plus one more for every partition that starts inside it, so prefix[r] = r + (number of
+// partitions that start inside a request before r).
 __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int parts,
                                                    int32_t* __restrict__ meta,
                                                    int32_t* __restrict__ prefix,
                                                    uint32_t* __restrict__ status) {
   (void)s_q;
-  if (threadIdx.x != 0) return;
-  status[0] = 0u;
-  status[1] = 0u;
-  const int nb = (topk + kTopkBlock - 1) / kTopkBlock;
-  const long long total = static_cast<long long>(b) * (nb + kFixedOverhead);
-  const long long payload = (total + parts - 1) / parts + kFixedOverhead;
-  int req = 0, blk = 0, slot = 0;
-  prefix[0] = 0;
-  for (int part = 0; part < parts; ++part) {
-    int32_t* m = meta + static_cast<size_t>(part) * kMetaInts;
-    if (req >= b) {
-      m[0] = b; m[1] = b; m[2] = 0; m[3] = 0; m[4] = slot; m[5] = 0; m[6] = 0; m[7] = 0;
-      continue;
-    }
-    long long remain = payload;
-    const int begin_req = req, begin_block = blk, begin_slot = slot;
-    const int first_split = blk > 0;
-    int end_req = req, end_block = blk, last_split = 0;
-    while (req < b) {
+  extern __shared__ __align__(16) int32_t sched_smem[];
+  int32_t* smeta = sched_smem;                                       // [parts][8]
+  int32_t* split_starts = sched_smem + static_cast<size_t>(parts) * kMetaInts;  // [parts]
+  __shared__ int n_starts;
+  griddep_launch_dependents();  // the decode pass may start its set-up; it waits for the plan
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    status[0] = 0u;
+    status[1] = 0u;
+    const int nb = (topk + kTopkBlock - 1) / kTopkBlock;
+    const long long cost = nb + kFixedOverhead;  // one whole request
+    const long long total = static_cast<long long>(b) * cost;
+    const long long payload = (total + parts - 1) / parts + kFixedOverhead;
+    int req = 0, blk = 0, slot = 0, ns = 0;
+    for (int part = 0; part < parts; ++part) {
+      int32_t* m = smeta + static_cast<size_t>(part) * kMetaInts;
+      if (req >= b) {
+        m[0] = b; m[1] = b; m[2] = 0; m[3] = 0; m[4] = slot; m[5] = 0; m[6] = 0; m[7] = 0;
+        continue;
+      }
+      long long remain = payload;
+      const int begin_req = req, begin_block = blk, begin_slot = slot;
+      const int first_split = blk > 0;
+      if (first_split) split_starts[ns++] = req;
+      int end_req = req, end_block = blk, last_split = 0;
       const int left = nb - blk;
-      if (left + kFixedOverhead <= remain) {  // the rest of this request fits
+      if (left + kFixedOverhead <= remain) {  // the rest of the current request fits
         remain -= left + kFixedOverhead;
         ++slot;
-        end_req = req; end_block = nb; last_split = 0;
+        end_req = req; end_block = nb;
         ++req; blk = 0;
-        prefix[req] = slot;
-        if (remain - kFixedOverhead <= 0) break;
-      } else {  // take what fits and split the request here
+        if (remain > kFixedOverhead && req < b) {
+          long long whole = (remain < 0x7FFFFFFF && cost < 0x7FFFFFFF)  // whole requests that fit
+                                ? static_cast<long long>(static_cast<uint32_t>(remain) /
+                                                         static_cast<uint32_t>(cost))
+                                : remain / cost;
+          if (whole > b - req) whole = b - req;
+          if (whole > 0) {
+            remain -= whole * cost;
+            slot += static_cast<int>(whole);
+            req += static_cast<int>(whole);
+            end_req = req - 1; end_block = nb;
+          }
+          if (req < b && remain > kFixedOverhead) {  // split the next request here
+            const int take = static_cast<int>(remain - kFixedOverhead);
+            ++slot;
+            blk = take;
+            end_req = req; end_block = take; last_split = 1;
+          }
+        }
+      } else {  // take what fits of the current request and split it here
         const long long take = remain - kFixedOverhead;
         if (take > 0) {
           ++slot;
           blk += static_cast<int>(take);
           end_req = req; end_block = blk; last_split = 1;
         }
-        break;
       }
+      m[0] = begin_req; m[1] = end_req; m[2] = begin_block; m[3] = end_block;
+      m[4] = begin_slot; m[5] = first_split; m[6] = last_split; m[7] = 0;
     }
-    m[0] = begin_req; m[1] = end_req; m[2] = begin_block; m[3] = end_block;
-    m[4] = begin_slot; m[5] = first_split; m[6] = last_split; m[7] = 0;
+    n_starts = ns;
   }
-  // Requests never reached (impossible with this payload, kept for safety): no split.
-  for (int r = req; r < b; ++r) prefix[r + 1] = slot;
+  __syncwarp();
+  const int4* src = reinterpret_cast<const int4*>(smeta);
+  int4* dst = reinterpret_cast<int4*>(meta);
+  for (int i = lane; i < parts * (kMetaInts / 4); i += 32) dst[i] = src[i];
+  const int ns = n_starts;
+  for (int r = lane; r <= b; r += 32) {
+    int lo = 0, hi = ns;  // number of entries < r (split_starts is ascending)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (split_starts[mid] < r) lo = mid + 1; else hi = mid;
+    }
+    prefix[r] = r + lo;
+  }
 }
 
 cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int32_t* prefix,
                          uint32_t* status, cudaStream_t stream) {
-  sched_kernel<<<1, 32, 0, stream>>>(b, s_q, topk, parts, meta, prefix, status);
+  const size_t smem = static_cast<size_t>(parts) * (kMetaInts + 1) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  sched_kernel<<<1, 32, smem, stream>>>(b, s_q, topk, parts, meta, prefix, status);
   return cudaGetLastError();
 }
 
