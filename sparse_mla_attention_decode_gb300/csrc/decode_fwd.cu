@@ -107,8 +107,14 @@ struct Ctx {
                                   (static_cast<uint32_t>(b) << 8) | parity);
   }
   // Bounded wait on an mbarrier phase of this CTA; false when the wait ran out or another
-  // role already gave up.
-  __device__ bool wait(int b, uint32_t parity, bool cluster_scope = false) const {
+  // role already gave up.  The first test is inline; the polling loop is out of line so that
+  // the many call sites keep the hot code small.
+  __device__ __forceinline__ bool wait(int b, uint32_t parity, bool cluster_scope = false) const {
+    const uint32_t a = bar(b);
+    if (cluster_scope ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+    return wait_slow(b, parity, cluster_scope);
+  }
+  __device__ __noinline__ bool wait_slow(int b, uint32_t parity, bool cluster_scope) const {
     const uint32_t a = bar(b);
     uint64_t deadline = 0;
     for (uint32_t i = 0;; ++i) {
@@ -344,7 +350,7 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase) {
       tc_fence_after();
       const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * KT_STAGE, 16, 1024, 2);
       const uint32_t d = tbase + TM_S + sb * BT;
-#pragma unroll
+#pragma unroll 4  // kept rolled: the issuing warp shares its instruction cache with the others
       for (int kk = 0; kk < 36; ++kk)  // descriptor start addresses advance in 16-byte units
         mma_ts(d, tbase + TM_Q + kk * 8, bdesc + ((((kk >> 2) * CHUNK) + (kk & 3) * 32) >> 4),
                IDESC_QK, kk > 0);
@@ -449,8 +455,6 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
 #pragma unroll
       for (int k = 0; k < BT / 16; ++k) tmem_ld16(ts + sb * BT + k * 16, sr + k * 16);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(c.bar(B_S_EMPTY + sb));
       // block max in base-2 units: fmaxf skips the NaN scores of invalid slots, and the scale
       // is positive, so it applies to the max of the raw scores (four chains for ILP)
       const float c2 = p.score_scale_log2;
@@ -472,20 +476,30 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       if (g >= NMSG && !c.wait_warp(B_MSG_FREE + st, ((g / NMSG) - 1) & 1, true)) goto out;
       const uint32_t msg = c.sbase + OFF_MSG + st * MSG_STRIDE;
       // p = 2^(s * c2 - mref); an invalid slot's NaN stays NaN through ex2 and fmaxf(NaN, 0)
-      // turns it into p = 0
+      // turns it into p = 0.  The scores are read again from tensor memory, 32 at a time, so
+      // this loop stays rolled (a small hot loop next to the other roles' code).
       float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r32[32];
+        tmem_ld16(ts + sb * BT + hh * 32, r32);
+        tmem_ld16(ts + sb * BT + hh * 32 + 16, r32 + 16);
+        tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t w[4];
+        for (int k = 0; k < 4; ++k) {
+          uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fmaxf(ex2(fmaf(__uint_as_float(sr[8 * k + 2 * e]), c2, -mref)), 0.f);
-          const float p1 = fmaxf(ex2(fmaf(__uint_as_float(sr[8 * k + 2 * e + 1]), c2, -mref)), 0.f);
-          sq[e] += p0 + p1;
-          w[e] = pack_f16x2(p0, p1);
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = fmaxf(ex2(fmaf(__uint_as_float(r32[8 * k + 2 * e]), c2, -mref)), 0.f);
+            const float p1 = fmaxf(ex2(fmaf(__uint_as_float(r32[8 * k + 2 * e + 1]), c2, -mref)), 0.f);
+            sq[e] += p0 + p1;
+            w[e] = pack_f16x2(p0, p1);
+          }
+          st_shared_v4(msg + sw128_chunk(i, 4 * hh + k), w[0], w[1], w[2], w[3]);
         }
-        st_shared_v4(msg + sw128_chunk(i, k), w[0], w[1], w[2], w[3]);
       }
+      tc_fence_before();
+      mbar_arrive(c.bar(B_S_EMPTY + sb));  // every read of this score buffer is done
       const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
       l = l * alpha + sum;
       st_shared_f32(msg + MSG_ALPHA + 4 * i, alpha);
