@@ -83,9 +83,15 @@ constexpr int OFF_STARTED = OFF_ABORT + 16;  // request ranges whose Q is staged
 constexpr int SMEM_BYTES = OFF_STARTED + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// warps: 0-3 softmax (S) / correction + epilogue (O); 4-11 gather + dequant; 12 MMA;
-// 13 message relay (O; idle on the S-CTA).
-constexpr int NTHREADS = 448;
+// warps: 0-3 softmax (S) / correction + epilogue (O); 5-7, 9-11, 13-14 gather + dequant;
+// 12 MMA; 8 message relay (O; idle on the S-CTA); 4 idle.  The SM sub-partition that issues
+// the MMAs (warps 0, 4, 8, 12) runs no dequant warp, so the single issuing thread is not
+// starved of issue slots while a tile is being converted.
+constexpr int NTHREADS = 480;
+__device__ __forceinline__ int dequant_index(int warp) {
+  if ((warp & 3) == 0 || warp < 5 || warp > 14) return -1;
+  return warp - 5 - ((warp - 4) >> 2);  // 5, 6, 7 -> 0, 1, 2; 9, 10, 11 -> 3, 4, 5; 13, 14 -> 6, 7
+}
 constexpr uint32_t TM_Q = 0, TM_S = 288;  // S-CTA columns; the O-CTA uses all 512 for O
 constexpr uint32_t IDESC_QK = umma_idesc_f16(128, BT, 0);
 constexpr uint32_t IDESC_PV = umma_idesc_f16(128, 256, 1);
@@ -173,7 +179,7 @@ struct Cursor {
 };
 
 // ---------------------------------------------------------------------------------------
-// Gather + dequant (warps 4-11 of both CTAs).  Warp w owns rows w, w + 8, ..., w + 56 of every
+// Gather + dequant (the eight dequant warps of both CTAs).  Dequant warp w owns rows w, w + 8, ..., w + 56 of every
 // block and handles them four at a time: the eight lanes 8 r .. 8 r + 7 share a row, and lane
 // j of the eight copies and converts 16-byte code chunks j, j + 8, j + 16, j + 24 of it
 // (dims [16 c, 16 c + 16) of chunk c) and, on the S-CTA, RoPE chunk j; lane 0 of the eight
@@ -697,13 +703,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const bool active = pl.begin_req < p.b;
 
   if (active) {
-    c.role = (scores ? 0u : 8u) + (warp < 4 ? 1u : warp < 12 ? 2u : warp == 12 ? 3u : 4u);
+    const int dq = dequant_index(warp);
+    c.role = (scores ? 0u : 8u) + (warp < 4 ? 1u : dq >= 0 ? 2u : warp == 12 ? 3u : 4u);
     if (warp < 4) {
       if (scores) role_softmax(p, c, pl, s, tbase, threadIdx.x);
       else role_values_epilogue(p, c, pl, s, tbase, threadIdx.x);
-    } else if (warp < 12) {
-      if (scores) role_dequant<true>(p, c, pl, s, threadIdx.x - 128);
-      else role_dequant<false>(p, c, pl, s, threadIdx.x - 128);
+    } else if (dq >= 0) {
+      if (scores) role_dequant<true>(p, c, pl, s, dq * 32 + lane);
+      else role_dequant<false>(p, c, pl, s, dq * 32 + lane);
     } else if (warp == 12) {
       if (lane == 0) {
         if (scores) role_mma_scores(c, pl, tbase);
@@ -711,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mma_commit(c.bar(B_DRAIN));  // every issued MMA has finished before TMEM is freed
         c.drain(B_DRAIN, 0);
       }
-    } else {
+    } else if (warp == 8) {
       if (!scores && lane == 0) role_relay(c, pl);
     }
   }
