@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/sparse_mla.h"
 #include "smla_internal.h"
@@ -26,6 +27,28 @@ smla_status check_dims(const smla_dims* d) {
   return SMLA_OK;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time dependency on libcuda).
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
 smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
   if (num_sms <= 0) {
     int dev = 0;
@@ -46,6 +69,18 @@ smla_status cuda_status(cudaError_t e) {
 }
 
 }  // namespace
+
+bool smla::encode_q_map(CUtensorMap* map, const void* q, int64_t tokens, int h_q) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDQk), static_cast<cuuint64_t>(tokens * h_q)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDQk) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(h_q)};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 extern "C" {
 
@@ -123,6 +158,7 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
   const PlanLayout L = plan_layout(dims->b, parts);
   const uint8_t* plan = static_cast<const uint8_t*>(sched_meta);
   DecodeParams p;
+  if (!encode_q_map(&p.q_map, q, tokens, dims->h_q)) return SMLA_ERR_CUDA;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv = static_cast<const uint8_t*>(kv_cache);
   p.indices = indices;

@@ -73,7 +73,9 @@ enum Bar {
   B_O_FULL = B_PV_DONE + NMSG,      // commit after the last PV of a range
   B_O_EMPTY = B_O_FULL + 1,         // 128 epilogue threads
   B_DRAIN = B_O_EMPTY + 1,          // MMA drain on the way out
-  B_STAGED = B_DRAIN + 1,           // [3] 128 softmax threads wrote a message slot (S-CTA)
+  B_STAGED = B_DRAIN + 1,           // [NMSG] 128 softmax threads wrote a message slot (S-CTA)
+  B_QLOAD = B_STAGED + NMSG,        // 1 expect-tx arrival + the bytes of the first token's Q rows
+  B_QREAD = B_QLOAD + 1,            // 128 softmax threads: Q read out of the key-tile region
   NUM_BARS
 };
 constexpr int OFF_BARS = OFF_MISC;
@@ -309,6 +311,8 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     const int32_t ixB = idx_of(fetch);      // block cur + 2, loaded one block early
     vmask |= valid_bits(ixA) << 8;
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
+    // the first token's Q passes through the key-tile region on its way to tensor memory
+    if (kScores && g == 0 && !c.wait_warp(B_QREAD, 0)) goto out;
     {
       const uint32_t tile = c.sbase + OFF_TILE + st * stage_bytes;
 #pragma unroll 1
@@ -396,6 +400,51 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
 }
 
 // ---------------------------------------------------------------------------------------
+// S-CTA, first token of the partition: its Q comes in by nine tiled tensor copies (one per
+// 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle) into the key-tile region, which no
+// tile uses yet, and thread i = head i converts its row to fp16 and writes it to tensor
+// memory.  The swizzle puts unit u of row r at position u ^ (r % 8), so eight consecutive
+// heads read eight distinct bank groups.  (Register loads of 147 KB would run at the SM's
+// scattered-load rate.)  False if a wait ran out.
+static_assert(9 * 128 * 128 <= OFF_MSG, "Q fits in the key-tile region");
+__device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
+                             uint32_t& bad) {
+  const uint32_t qs = c.sbase + OFF_TILE;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
+  if (i == 0) {
+    mbar_arrive_expect_tx(c.bar(B_QLOAD), 9 * chunk_bytes);
+    for (int ch = 0; ch < 9; ++ch)
+      tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD));
+  }
+  if (!c.wait_warp(B_QLOAD, 0)) return false;
+  const bool live = i < p.h_q;
+  const uint32_t row = qs + (live ? i : 0) * 128;
+  const uint32_t sw = static_cast<uint32_t>(i & 7);
+#pragma unroll 1
+  for (int cc = 0; cc < 18; ++cc) {  // 18 x 32 dims = 18 x 16 columns
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + k);
+      uint32_t in[4];
+      ld_shared_v4(row + (cc >> 1) * chunk_bytes + ((u ^ sw) << 4), in[0], in[1], in[2], in[3]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t r = pack_f16x2(__uint_as_float(in[e] << 16),
+                                      __uint_as_float(in[e] & 0xFFFF0000u));
+        bad |= ((r & 0x7C00u) == 0x7C00u) | ((r & 0x7C000000u) == 0x7C000000u);
+        w[4 * k + e] = live ? r : 0u;
+      }
+    }
+    tmem_st16(tq + cc * 16, w);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(c.bar(B_Q_FULL));
+  mbar_arrive(c.bar(B_QREAD));  // this thread is done with the key-tile region
+  return true;
+}
+
 // S-CTA: Q of one query token into tensor memory (fp16, two dims per column), thread i = head i.
 __device__ void stage_q(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
                         uint32_t& bad) {
@@ -447,9 +496,19 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   uint32_t g = 0;
   volatile uint32_t* started = reinterpret_cast<volatile uint32_t*>(
       __cvta_shared_to_generic(c.sbase + OFF_STARTED));
-  stage_q(p, c, tq, pl.begin_req * p.s_q + s, i, qbad);
+  // Thread i pulls its head's Q row (1152 bytes = 9 lines) of a token into L2 ahead of the
+  // staging loads, whose later batches then hit L2.
+  auto prefetch_q = [&](int tok) {
+    if (i < p.h_q) {
+      const uint8_t* row = reinterpret_cast<const uint8_t*>(p.q + (static_cast<size_t>(tok) * p.h_q + i) * kDQk);
+#pragma unroll
+      for (int k = 0; k < 9; ++k) prefetch_l2(row + k * 128);
+    }
+  };
+  if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + s, i, qbad)) goto out;
   for (int req = pl.begin_req; req <= pl.end_req; ++req) {
     if (i == 0) *started = static_cast<uint32_t>(req - pl.begin_req + 1);
+    if (req < pl.end_req) prefetch_q((req + 1) * p.s_q + s);  // staged after this range
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     float m = -INFINITY;  // running max (base-2 units) used as the exponent reference
     float l = 0.f;        // running exp-sum against m
@@ -638,7 +697,7 @@ __device__ void role_relay(const Ctx& c, const Plan& pl) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    decode_kernel(const DecodeParams p) {
+    decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -675,6 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(c.bar(B_S_EMPTY + b), 128);
     }
     mbar_init(c.bar(B_Q_FULL), 128);
+    mbar_init(c.bar(B_QLOAD), 1);
+    mbar_init(c.bar(B_QREAD), 128);
     mbar_init(c.bar(B_O_FULL), 1);
     mbar_init(c.bar(B_O_EMPTY), 128);
     mbar_init(c.bar(B_DRAIN), 1);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the host runtime and the kernels of libsparse_mla.so.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -45,6 +46,9 @@ inline AccumLayout accum_layout(int b, int s_q, int h_q, int parts) {
 }
 
 struct DecodeParams {
+  // Q as a 2-D tensor (rows = token * h_q + head, 576 bf16 columns), box 64 columns x h_q rows,
+  // 128-byte swizzle: one box is one 64-dim chunk of a token's Q in the SW128 K-major layout.
+  alignas(64) CUtensorMap q_map;
   const __nv_bfloat16* q;   // [b][s_q][h_q][576]
   const uint8_t* kv;        // [num_rows][656]
   const int32_t* indices;   // [b][s_q][topk]
@@ -68,6 +72,9 @@ struct CombineParams {
   float* lse;
   int b, s_q, h_q;
 };
+
+// Encodes DecodeParams::q_map for q (host; false if the driver call is missing or fails).
+bool encode_q_map(CUtensorMap* map, const void* q, int64_t tokens, int h_q);
 
 // Kernel launchers (return the launch's cudaError_t).
 cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int32_t* prefix,
