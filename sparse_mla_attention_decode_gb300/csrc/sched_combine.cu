@@ -20,78 +20,181 @@ namespace smla {
 // splits per request.  Split slots are numbered in partition order, so the splits of one
 // request are consecutive and prefix[req] is the slot of its first split.
 //
-// Every request has the same ceil(topk / 64) blocks, so one partition's walk is a few lines of
-// arithmetic: finish the current request if it fits, then as many whole requests as the
-// remaining capacity holds, then split the next one.  Lane 0 walks the partitions in order
-// into shared memory (one thread's global stores would issue one by one); the warp then copies
-// the table out with 16-byte stores and fills the split prefix: a request r has one split
-// plus one more for every partition that starts inside it, so prefix[r] = r + (number of
+// Every request has the same nb = ceil(topk / 64) blocks and every partition the same
+// payload, so the walk of one partition depends only on the block it starts at (and on the
+// number of requests left).  The warp tabulates that walk for every start block in parallel;
+// lane 0 then steps through the partitions with one table lookup each (falling back to the
+// exact walk where the last requests cap it), staging the table in shared memory; the warp
+// copies it out with 16-byte stores and fills the split prefix: a request r has one split plus
+// one more for every partition that starts inside it, so prefix[r] = r + (number of
 // partitions that start inside a request before r).
+struct __align__(16) PartWalk {
+  int end_req, end_block;    // last request touched (relative to the first) and its end block
+  int last_split, reach;     // split at the end; furthest request touched (relative)
+  int next_req, next_block;  // where the next partition starts (relative request, block)
+  int slots, pad;            // splits this partition contributes
+};
+
+// One partition starting at block blk of request 0, with `left_reqs` requests available
+// (the greedy rule: finish the current request if it fits, then whole requests, then split).
+__device__ __forceinline__ PartWalk walk_partition(int nb, long long payload, int blk,
+                                                    long long left_reqs) {
+  const long long cost = nb + kFixedOverhead;
+  PartWalk w;
+  long long remain = payload;
+  const int left = nb - blk;
+  if (left + kFixedOverhead <= remain) {  // the rest of the current request fits
+    remain -= left + kFixedOverhead;
+    long long req = 1;
+    w.end_req = 0; w.end_block = nb; w.slots = 1; w.last_split = 0;
+    w.next_req = 1; w.next_block = 0;
+    if (remain > kFixedOverhead && req < left_reqs) {
+      // Whole requests that fit: the greedy takes one while it fits and stops once at most
+      // the overhead is left, which is floor(remain / cost) when a request costs more than the
+      // overhead (nb >= 1) and floor((remain - 1) / cost) when it costs exactly that (nb = 0).
+      const long long num = cost > kFixedOverhead ? remain : remain - 1;
+      long long whole = (num < 0x7FFFFFFF && cost < 0x7FFFFFFF)
+                            ? static_cast<long long>(static_cast<uint32_t>(num) /
+                                                     static_cast<uint32_t>(cost))
+                            : num / cost;
+      if (whole > left_reqs - req) whole = left_reqs - req;
+      if (whole > 0) {
+        remain -= whole * cost;
+        req += whole;
+        w.slots += static_cast<int>(whole);
+        w.end_req = static_cast<int>(req - 1); w.end_block = nb;
+        w.next_req = static_cast<int>(req);
+      }
+      if (req < left_reqs && remain > kFixedOverhead) {  // split the next request here
+        const int take = static_cast<int>(remain - kFixedOverhead);
+        w.slots += 1;
+        w.end_req = static_cast<int>(req); w.end_block = take; w.last_split = 1;
+        w.next_req = static_cast<int>(req); w.next_block = take;
+      }
+    }
+  } else {  // take what fits of the current request and split it here
+    const int take = static_cast<int>(remain - kFixedOverhead);  // >= 1: payload > 5
+    w.end_req = 0; w.end_block = blk + take; w.slots = 1; w.last_split = 1;
+    w.next_req = 0; w.next_block = blk + take;
+  }
+  w.reach = w.next_block > 0 ? w.next_req : w.end_req;
+  w.pad = 0;
+  return w;
+}
+
+// levels >= 0: the jump tables of 2^k partitions (k < levels, 2^levels >= parts) fit in shared
+// memory and every lane finds the start of its partitions by pointer jumping; levels < 0: lane
+// 0 walks all partitions in order.
 __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int parts,
-                                                   int32_t* __restrict__ meta,
+                                                   int levels, int32_t* __restrict__ meta,
                                                    int32_t* __restrict__ prefix,
                                                    uint32_t* __restrict__ status) {
   (void)s_q;
   extern __shared__ __align__(16) int32_t sched_smem[];
-  int32_t* smeta = sched_smem;                                       // [parts][8]
-  int32_t* split_starts = sched_smem + static_cast<size_t>(parts) * kMetaInts;  // [parts]
+  const int nb = (topk + kTopkBlock - 1) / kTopkBlock;
+  const int nlev = levels > 0 ? levels : 0;
+  PartWalk* table = reinterpret_cast<PartWalk*>(sched_smem);                   // [nb]
+  int4* jump = reinterpret_cast<int4*>(table + nb);  // [nlev][nb]: {next block, +requests, +splits}
+  int4* states = jump + static_cast<size_t>(nlev) * nb;  // [parts] (levels >= 0): {req, block, slot}
+  int32_t* smeta = reinterpret_cast<int32_t*>(states + (levels >= 0 ? parts : 0));  // [parts][8]
+  int32_t* split_starts = smeta + static_cast<size_t>(parts) * kMetaInts;       // [parts]
+  int4* m4 = reinterpret_cast<int4*>(smeta);
   __shared__ int n_starts;
   griddep_launch_dependents();  // the decode pass may start its set-up; it waits for the plan
   const int lane = threadIdx.x;
+  const long long total = static_cast<long long>(b) * (nb + kFixedOverhead);
+  const long long payload = (total + parts - 1) / parts + kFixedOverhead;
+  constexpr long long kUncapped = 0x7FFFFFFFFFFFll;
+  for (int blk = lane; blk < nb; blk += 32) {
+    const PartWalk w = walk_partition(nb, payload, blk, kUncapped);
+    table[blk] = w;
+    if (nlev > 0) jump[blk] = make_int4(w.next_block, w.next_req, w.slots, 0);
+  }
+  __syncwarp();
+  for (int k = 1; k < nlev; ++k) {  // jump[k] = two jumps of jump[k - 1]
+    for (int blk = lane; blk < nb; blk += 32) {
+      const int4 x = jump[(k - 1) * nb + blk];
+      const int4 y = jump[(k - 1) * nb + x.x];
+      jump[k * nb + blk] = make_int4(y.x, x.y + y.y, x.z + y.z, 0);
+    }
+    __syncwarp();
+  }
+  // The plan buffer may still be read by the kernels of the previous decode on this stream:
+  // write nothing before they are done (this launch may start early).
+  griddep_wait();
   if (lane == 0) {
     status[0] = 0u;
     status[1] = 0u;
-    const int nb = (topk + kTopkBlock - 1) / kTopkBlock;
-    const long long cost = nb + kFixedOverhead;  // one whole request
-    const long long total = static_cast<long long>(b) * cost;
-    const long long payload = (total + parts - 1) / parts + kFixedOverhead;
-    int req = 0, blk = 0, slot = 0, ns = 0;
-    for (int part = 0; part < parts; ++part) {
-      int32_t* m = smeta + static_cast<size_t>(part) * kMetaInts;
+  }
+  int first = 0;  // first partition taken by the exact walk below
+  int ns = 0;
+  if (levels >= 0) {
+    // start of partition p = p applications of the (uncapped) one-partition walk to (0, 0, 0)
+    for (int p = lane; p < parts; p += 32) {
+      int req = 0, blk = 0, slot = 0;
+      for (int k = 0; k < nlev; ++k)
+        if ((p >> k) & 1) {
+          const int4 e = jump[k * nb + blk];
+          req += e.y;
+          slot += e.z;
+          blk = e.x;
+        }
+      states[p] = make_int4(req, blk, slot, 0);
+    }
+    __syncwarp();
+    // the first partition that is empty or whose walk the last requests may cap
+    first = parts;
+    for (int base = 0; base < parts && first == parts; base += 32) {
+      const int p = base + lane;
+      bool need = false;
+      if (p < parts) {
+        const int4 st = states[p];
+        need = st.x >= b || st.x + table[st.y].reach >= b - 1;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, need);
+      if (m) first = base + __ffs(m) - 1;
+    }
+    // partitions before it, in parallel; the split starts are compacted in partition order
+    for (int base = 0; base < first; base += 32) {
+      const int p = base + lane;
+      bool fs = false;
+      int4 st = make_int4(0, 0, 0, 0);
+      if (p < first) {
+        st = states[p];
+        const PartWalk& w = table[st.y];
+        fs = st.y > 0;
+        m4[2 * p] = make_int4(st.x, st.x + w.end_req, st.y, w.end_block);
+        m4[2 * p + 1] = make_int4(st.z, fs ? 1 : 0, w.last_split, 0);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, fs);
+      if (fs) split_starts[ns + __popc(m & ((1u << lane) - 1u))] = st.x;
+      ns += __popc(m);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    int req = 0, blk = 0, slot = 0;
+    if (first > 0 && first < parts) {
+      const int4 st = states[first];
+      req = st.x; blk = st.y; slot = st.z;
+    }
+    for (int part = first; part < parts; ++part) {
       if (req >= b) {
-        m[0] = b; m[1] = b; m[2] = 0; m[3] = 0; m[4] = slot; m[5] = 0; m[6] = 0; m[7] = 0;
+        m4[2 * part] = make_int4(b, b, 0, 0);
+        m4[2 * part + 1] = make_int4(slot, 0, 0, 0);
         continue;
       }
-      long long remain = payload;
-      const int begin_req = req, begin_block = blk, begin_slot = slot;
+      PartWalk w;
+      if (nb > 0) w = table[blk];
+      // near the end the number of requests left may cap the walk: take it exactly there
+      if (nb == 0 || req + w.reach >= b - 1) w = walk_partition(nb, payload, blk, b - req);
       const int first_split = blk > 0;
       if (first_split) split_starts[ns++] = req;
-      int end_req = req, end_block = blk, last_split = 0;
-      const int left = nb - blk;
-      if (left + kFixedOverhead <= remain) {  // the rest of the current request fits
-        remain -= left + kFixedOverhead;
-        ++slot;
-        end_req = req; end_block = nb;
-        ++req; blk = 0;
-        if (remain > kFixedOverhead && req < b) {
-          long long whole = (remain < 0x7FFFFFFF && cost < 0x7FFFFFFF)  // whole requests that fit
-                                ? static_cast<long long>(static_cast<uint32_t>(remain) /
-                                                         static_cast<uint32_t>(cost))
-                                : remain / cost;
-          if (whole > b - req) whole = b - req;
-          if (whole > 0) {
-            remain -= whole * cost;
-            slot += static_cast<int>(whole);
-            req += static_cast<int>(whole);
-            end_req = req - 1; end_block = nb;
-          }
-          if (req < b && remain > kFixedOverhead) {  // split the next request here
-            const int take = static_cast<int>(remain - kFixedOverhead);
-            ++slot;
-            blk = take;
-            end_req = req; end_block = take; last_split = 1;
-          }
-        }
-      } else {  // take what fits of the current request and split it here
-        const long long take = remain - kFixedOverhead;
-        if (take > 0) {
-          ++slot;
-          blk += static_cast<int>(take);
-          end_req = req; end_block = blk; last_split = 1;
-        }
-      }
-      m[0] = begin_req; m[1] = end_req; m[2] = begin_block; m[3] = end_block;
-      m[4] = begin_slot; m[5] = first_split; m[6] = last_split; m[7] = 0;
+      m4[2 * part] = make_int4(req, req + w.end_req, blk, w.end_block);
+      m4[2 * part + 1] = make_int4(slot, first_split, w.last_split, 0);
+      slot += w.slots;
+      req += w.next_req;
+      blk = w.next_block;
     }
     n_starts = ns;
   }
@@ -99,7 +202,7 @@ __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int
   const int4* src = reinterpret_cast<const int4*>(smeta);
   int4* dst = reinterpret_cast<int4*>(meta);
   for (int i = lane; i < parts * (kMetaInts / 4); i += 32) dst[i] = src[i];
-  const int ns = n_starts;
+  ns = n_starts;
   for (int r = lane; r <= b; r += 32) {
     int lo = 0, hi = ns;  // number of entries < r (split_starts is ascending)
     while (lo < hi) {
@@ -112,14 +215,35 @@ __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int
 
 cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int32_t* prefix,
                          uint32_t* status, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(parts) * (kMetaInts + 1) * sizeof(int32_t);
+  const size_t nb = static_cast<size_t>((topk + kTopkBlock - 1) / kTopkBlock);
+  int levels = 0;
+  while ((1 << levels) < parts) ++levels;
+  const size_t base = nb * sizeof(PartWalk) + static_cast<size_t>(parts) * (kMetaInts + 1) * 4;
+  const size_t fast = base + static_cast<size_t>(levels) * nb * 16 + static_cast<size_t>(parts) * 16;
+  size_t smem = base;
+  if (nb > 0 && fast <= 48 * 1024) {
+    smem = fast;
+  } else {
+    levels = -1;
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  sched_kernel<<<1, 32, smem, stream>>>(b, s_q, topk, parts, meta, prefix, status);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the launch overlaps the tail of the preceding kernel;
+  // griddepcontrol.wait inside holds every write until that kernel is done.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sched_kernel, b, s_q, topk, parts, levels, meta, prefix, status);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -48,7 +48,7 @@ inline AccumLayout accum_layout(int b, int s_q, int h_q, int parts) {
 struct DecodeParams {
   // Q as a 2-D tensor (rows = token * h_q + head, 576 bf16 columns), box 64 columns x h_q rows,
   // 128-byte swizzle: one box is one 64-dim chunk of a token's Q in the SW128 K-major layout.
-  alignas(64) CUtensorMap q_map;
+  CUtensorMap q_map;  // (the type is 64-byte aligned)
   const __nv_bfloat16* q;   // [b][s_q][h_q][576]
   const uint8_t* kv;        // [num_rows][656]
   const int32_t* indices;   // [b][s_q][topk]

@@ -42,7 +42,11 @@ def _full(wl, num_sms, what):
 @pytest.mark.parametrize("b,s_q,topk,num_sms", [(2, 1, 128, 132), (64, 1, 2048, 152),
                                                 (32, 1, 2048, 152), (128, 2, 2048, 152),
                                                 (1, 4096, 2048, 152), (3, 1, 100, 14),
-                                                (7, 3, 1000, 40), (200, 1, 64, 6)])
+                                                (7, 3, 1000, 40), (200, 1, 64, 6),
+                                                (5, 1, 0, 16), (9, 1, 0, 152), (1, 1, 1, 152),
+                                                (76, 1, 2048, 152), (77, 1, 2048, 152),
+                                                (50, 1, 320, 8), (13, 2, 64, 200),
+                                                (64, 1, 4096, 152), (300, 1, 2048, 152)])
 def test_sched_meta_matches_oracle(dev, b, s_q, topk, num_sms):
     import sparse_mla_attention_decode_gb300 as smla
     op = smla.SparseMLADecode(b, s_q, 128, topk, 16, device=dev, num_sms=num_sms)
