@@ -81,8 +81,7 @@ enum Bar {
 constexpr int OFF_BARS = OFF_MISC;
 constexpr int OFF_TMEM_SLOT = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 16;
-constexpr int OFF_STARTED = OFF_ABORT + 16;  // request ranges whose Q is staged (S-CTA)
-constexpr int SMEM_BYTES = OFF_STARTED + 16 + 1024;  // + alignment slack
+constexpr int SMEM_BYTES = OFF_ABORT + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // warps: 0-3 softmax (S) / correction + epilogue (O); 5-7, 9-11, 13-14 gather + dequant;
@@ -311,8 +310,11 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     const int32_t ixB = idx_of(fetch);      // block cur + 2, loaded one block early
     vmask |= valid_bits(ixA) << 8;
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
-    // the first token's Q passes through the key-tile region on its way to tensor memory
-    if (kScores && g == 0 && !c.wait_warp(B_QREAD, 0)) goto out;
+    // each token's Q passes through the key-tile region on its way to tensor memory: the
+    // first tile of a request waits until it has been read out
+    if (kScores && cur.blk == pl.first_block(cur.req) &&
+        !c.wait_warp(B_QREAD, static_cast<uint32_t>(cur.req - pl.begin_req) & 1u))
+      goto out;
     {
       const uint32_t tile = c.sbase + OFF_TILE + st * stage_bytes;
 #pragma unroll 1
@@ -400,15 +402,17 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
 }
 
 // ---------------------------------------------------------------------------------------
-// S-CTA, first token of the partition: its Q comes in by nine tiled tensor copies (one per
-// 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle) into the key-tile region, which no
-// tile uses yet, and thread i = head i converts its row to fp16 and writes it to tensor
-// memory.  The swizzle puts unit u of row r at position u ^ (r % 8), so eight consecutive
-// heads read eight distinct bank groups.  (Register loads of 147 KB would run at the SM's
-// scattered-load rate.)  False if a wait ran out.
+// S-CTA: the Q of one query token (request number `item` of the partition) comes in by nine
+// tiled tensor copies (one per 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle) into the
+// key-tile region, and thread i = head i converts its row to fp16 and writes it to tensor
+// memory.  The region is free then: every QK of the previous request has completed and the
+// dequant warps hold the request's first tile back until B_QREAD.  The swizzle puts unit u of
+// row r at position u ^ (r % 8), so eight consecutive heads read eight distinct bank groups.
+// (Register loads of 147 KB would run at the SM's scattered-load rate.)  False if a wait ran
+// out.
 static_assert(9 * 128 * 128 <= OFF_MSG, "Q fits in the key-tile region");
 __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
-                             uint32_t& bad) {
+                             uint32_t& bad, uint32_t item) {
   const uint32_t qs = c.sbase + OFF_TILE;
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
   if (i == 0) {
@@ -416,7 +420,7 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
     for (int ch = 0; ch < 9; ++ch)
       tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD));
   }
-  if (!c.wait_warp(B_QLOAD, 0)) return false;
+  if (!c.wait_warp(B_QLOAD, item & 1)) return false;
   const bool live = i < p.h_q;
   const uint32_t row = qs + (live ? i : 0) * 128;
   const uint32_t sw = static_cast<uint32_t>(i & 7);
@@ -445,44 +449,6 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
   return true;
 }
 
-// S-CTA: Q of one query token into tensor memory (fp16, two dims per column), thread i = head i.
-__device__ void stage_q(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
-                        uint32_t& bad) {
-  const bool live = i < p.h_q;
-  const uint4* src = reinterpret_cast<const uint4*>(
-      p.q + (static_cast<size_t>(tok) * p.h_q + (live ? i : 0)) * kDQk);
-#pragma unroll 1
-  for (int batch = 0; batch < 3; ++batch) {  // 3 x 192 dims: all loads of a batch in flight
-    uint4 v[24];
-#pragma unroll
-    for (int k = 0; k < 24; ++k)
-      v[k] = ldg_v4(src + batch * 24 + k);  // rows past h_q read head 0 and are zeroed below
-#pragma unroll
-    for (int cc = 0; cc < 6; ++cc) {  // 6 x 32 dims = 6 x 16 columns
-      uint32_t w[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t in[4] = {v[cc * 4 + k].x, v[cc * 4 + k].y, v[cc * 4 + k].z, v[cc * 4 + k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t r = pack_f16x2(__uint_as_float(in[e] << 16),
-                                        __uint_as_float(in[e] & 0xFFFF0000u));
-          bad |= ((r & 0x7C00u) == 0x7C00u) | ((r & 0x7C000000u) == 0x7C000000u);
-          w[4 * k + e] = r;
-        }
-      }
-      if (!live) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = 0u;
-    }
-    tmem_st16(tq + (batch * 6 + cc) * 16, w);
-    }
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  mbar_arrive(c.bar(B_Q_FULL));
-}
-
 // S-CTA softmax warpgroup: thread i owns head row i (tensor-memory lane i).
 __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl, int s,
                              uint32_t tbase, int i) {
@@ -494,21 +460,8 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   const bool live = i < p.h_q;
   uint32_t qbad = 0;
   uint32_t g = 0;
-  volatile uint32_t* started = reinterpret_cast<volatile uint32_t*>(
-      __cvta_shared_to_generic(c.sbase + OFF_STARTED));
-  // Thread i pulls its head's Q row (1152 bytes = 9 lines) of a token into L2 ahead of the
-  // staging loads, whose later batches then hit L2.
-  auto prefetch_q = [&](int tok) {
-    if (i < p.h_q) {
-      const uint8_t* row = reinterpret_cast<const uint8_t*>(p.q + (static_cast<size_t>(tok) * p.h_q + i) * kDQk);
-#pragma unroll
-      for (int k = 0; k < 9; ++k) prefetch_l2(row + k * 128);
-    }
-  };
-  if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + s, i, qbad)) goto out;
+  if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + s, i, qbad, 0)) goto out;
   for (int req = pl.begin_req; req <= pl.end_req; ++req) {
-    if (i == 0) *started = static_cast<uint32_t>(req - pl.begin_req + 1);
-    if (req < pl.end_req) prefetch_q((req + 1) * p.s_q + s);  // staged after this range
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     float m = -INFINITY;  // running max (base-2 units) used as the exponent reference
     float l = 0.f;        // running exp-sum against m
@@ -592,7 +545,10 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       }
     }
     // every QK^T of this range has completed: stage the next query token's Q
-    if (req < pl.end_req) stage_q(p, c, tq, (req + 1) * p.s_q + s, i, qbad);
+    if (req < pl.end_req &&
+        !stage_q_bulk(p, c, tq, (req + 1) * p.s_q + s, i, qbad,
+                      static_cast<uint32_t>(req + 1 - pl.begin_req)))
+      goto out;
   }
 out:
   if (qbad) atomicOr(c.status, SMLA_DEV_Q_RANGE);
@@ -728,7 +684,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(c.bar(B_PV_DONE + b), 1);
       mbar_init(c.bar(B_STAGED + b), 128);
     }
-    *reinterpret_cast<volatile uint32_t*>(sm + OFF_STARTED) = 0u;
     for (int b = 0; b < NSBUF; ++b) {
       mbar_init(c.bar(B_S_FULL + b), 1);
       mbar_init(c.bar(B_S_EMPTY + b), 128);

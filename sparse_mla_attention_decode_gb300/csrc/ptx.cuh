@@ -103,9 +103,6 @@ __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uin
       "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // ------------------------------------------------------------------ cluster / DSMEM
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -259,15 +256,6 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                : "memory");
 }
 
-// Global loads kept at their program point (volatile), so a software look-ahead is not sunk
-// to the first use by the compiler.
-__device__ __forceinline__ uint4 ldg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 // Asynchronous 16-byte global -> shared copy that bypasses L1 (cp.async, one per lane).  The
 // data does not pass through registers, so a warp can keep many row copies in flight.  With
 // src_bytes = 0 nothing is read and the 16 bytes are zero-filled.
