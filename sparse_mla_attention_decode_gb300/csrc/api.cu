@@ -70,16 +70,19 @@ smla_status cuda_status(cudaError_t e) {
 
 }  // namespace
 
-bool smla::encode_q_map(CUtensorMap* map, const void* q, int64_t tokens, int h_q) {
+bool smla::encode_rows_map(CUtensorMap* map, const void* base, bool fp32, int64_t rows, int cols,
+                           int box_cols, int box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDQk), static_cast<cuuint64_t>(tokens * h_q)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDQk) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(h_q)};
+  const cuuint64_t esize = fp32 ? 4 : 2;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box,
-             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 extern "C" {
@@ -158,7 +161,12 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
   const PlanLayout L = plan_layout(dims->b, parts);
   const uint8_t* plan = static_cast<const uint8_t*>(sched_meta);
   DecodeParams p;
-  if (!encode_q_map(&p.q_map, q, tokens, dims->h_q)) return SMLA_ERR_CUDA;
+  if (!encode_rows_map(&p.q_map, q, false, tokens * dims->h_q, kDQk, 64, dims->h_q) ||
+      !encode_rows_map(&p.out_map, out, false, tokens * dims->h_q, kDV, 64, dims->h_q) ||
+      !encode_rows_map(&p.acc_map, static_cast<uint8_t*>(workspace) + A.o_off, true,
+                       static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q, kDV, 32,
+                       dims->h_q))
+    return SMLA_ERR_CUDA;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv = static_cast<const uint8_t*>(kv_cache);
   p.indices = indices;
@@ -174,6 +182,7 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
   p.h_q = dims->h_q;
   p.topk = dims->topk;
   p.num_rows = static_cast<int>(dims->num_blocks * kPage);
+  p.store32 = aligned(out, 32) && aligned(workspace, 32) ? 1 : 0;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 / 256.0);
   return cuda_status(launch_decode(p, parts, s));
 }

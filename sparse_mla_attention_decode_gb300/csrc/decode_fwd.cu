@@ -76,6 +76,8 @@ enum Bar {
   B_STAGED = B_DRAIN + 1,           // [NMSG] 128 softmax threads wrote a message slot (S-CTA)
   B_QLOAD = B_STAGED + NMSG,        // 1 expect-tx arrival + the bytes of the first token's Q rows
   B_QREAD = B_QLOAD + 1,            // 128 softmax threads: Q read out of the key-tile region
+  B_OSTAGE = B_QREAD + 1,           // [8] 128 epilogue threads staged one output box (O-CTA)
+  B_OFREE = B_OSTAGE + 8,           // the stores have read the staging tiles (O-CTA)
   NUM_BARS
 };
 constexpr int OFF_BARS = OFF_MISC;
@@ -85,9 +87,9 @@ constexpr int SMEM_BYTES = OFF_ABORT + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // warps: 0-3 softmax (S) / correction + epilogue (O); 5-7, 9-11, 13-14 gather + dequant;
-// 12 MMA; 8 message relay (O; idle on the S-CTA); 4 idle.  The SM sub-partition that issues
-// the MMAs (warps 0, 4, 8, 12) runs no dequant warp, so the single issuing thread is not
-// starved of issue slots while a tile is being converted.
+// 12 MMA; 8 message relay (O; idle on the S-CTA); 4 output store issuer (O; idle on the
+// S-CTA).  The SM sub-partition that issues the MMAs (warps 0, 4, 8, 12) runs no dequant warp,
+// so the single issuing thread is not starved of issue slots while a tile is being converted.
 constexpr int NTHREADS = 480;
 __device__ __forceinline__ int dequant_index(int warp) {
   if ((warp & 3) == 0 || warp < 5 || warp > 14) return -1;
@@ -555,6 +557,163 @@ out:
 }
 
 // ---------------------------------------------------------------------------------------
+// O-CTA epilogue: writes O row `head` (a lane of this warp's tensor-memory quarter) for columns
+// [32 c0, 32 c1), scaled by invl: bf16 into out (unsplit request) or fp32 into the split's
+// partial.  The tensor-memory loads of the next 32 columns are in flight while the current 32
+// are scaled, converted and stored (32-byte stores when the buffers are aligned for them).
+__device__ void drain_o(const DecodeParams& p, uint32_t to, int head, bool no_split, int split,
+                        int tok, int s, float invl, int c0, int c1) {
+  const bool live = head < p.h_q;
+  uint8_t* dst_row =
+      no_split ? reinterpret_cast<uint8_t*>(p.out + (static_cast<size_t>(tok) * p.h_q + (live ? head : 0)) * kDV)
+               : reinterpret_cast<uint8_t*>(p.o_accum + ((static_cast<size_t>(split) * p.s_q + s) * p.h_q + (live ? head : 0)) * kDV);
+  auto store_chunk = [&](const uint32_t (&o)[32], int k) {  // columns [32 k, 32 k + 32)
+    if (!live) return;
+    if (no_split) {
+      uint32_t v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        v[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * invl, __uint_as_float(o[2 * e + 1]) * invl);
+      uint8_t* d = dst_row + k * 64;
+      if (p.store32) {
+        st_global_v8(d, *reinterpret_cast<const uint32_t(*)[8]>(v));
+        st_global_v8(d + 32, *reinterpret_cast<const uint32_t(*)[8]>(v + 8));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st_global_v4(d + 16 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+    } else {
+      uint32_t v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(o[e]) * invl);
+      uint8_t* d = dst_row + k * 128;
+      if (p.store32) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st_global_v8(d + 32 * e, *reinterpret_cast<const uint32_t(*)[8]>(v + 8 * e));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) st_global_v4(d + 16 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+    }
+  };
+  uint32_t oa[32], ob[32];
+  tmem_ld16(to + c0 * 32, oa);
+  tmem_ld16(to + c0 * 32 + 16, oa + 16);
+#pragma unroll 1
+  for (int k = c0; k < c1; k += 2) {
+    tmem_wait_ld();  // columns of chunk k are in oa
+    tmem_ld16(to + (k + 1) * 32, ob);
+    tmem_ld16(to + (k + 1) * 32 + 16, ob + 16);
+    store_chunk(oa, k);
+    tmem_wait_ld();  // chunk k + 1 in ob
+    if (k + 2 < c1) {
+      tmem_ld16(to + (k + 2) * 32, oa);
+      tmem_ld16(to + (k + 2) * 32 + 16, oa + 16);
+    }
+    store_chunk(ob, k + 1);
+  }
+}
+
+// O-CTA epilogue of the partition's last range: the rows go through the (now unused) value-tile
+// region in the 128-byte-swizzled box layout of the output's tensor map and leave by tiled TMA
+// stores, so the store traffic is whole lines instead of one 32-byte piece per row and lane.
+// bf16 output: one pass of 8 boxes (64 columns x h_q rows); fp32 split partial: two passes of 8
+// boxes (32 columns each).  Thread `head` converts its own row and arrives on the box's barrier
+// once its part of a box is written; the store issuer (role_store_issuer) sends each box as
+// soon as all rows are in, so the stores overlap the conversion.  False if a wait ran out.
+constexpr uint32_t OBOX = 16384;  // 128 rows x 128 bytes
+__device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, int head,
+                            bool no_split, float invl) {
+  const uint32_t stage = c.sbase + OFF_TILE;
+  const bool live = head < p.h_q;
+  const uint32_t row = stage + static_cast<uint32_t>(head) * 128;
+  const uint32_t sw = static_cast<uint32_t>(head & 7);
+  const int passes = no_split ? 1 : 2;
+  auto stage_chunk = [&](const uint32_t (&o)[32], int k) {  // columns [32 k, 32 k + 32)
+    if (live) {
+      if (no_split) {  // 4 units of 8 bf16; box k / 2, units (k % 2) * 4 + e
+        const uint32_t base = row + (k >> 1) * OBOX;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t u = static_cast<uint32_t>((k & 1) * 4 + e);
+          st_shared_v4(base + ((u ^ sw) << 4),
+                       pack_bf16x2(__uint_as_float(o[8 * e + 0]) * invl, __uint_as_float(o[8 * e + 1]) * invl),
+                       pack_bf16x2(__uint_as_float(o[8 * e + 2]) * invl, __uint_as_float(o[8 * e + 3]) * invl),
+                       pack_bf16x2(__uint_as_float(o[8 * e + 4]) * invl, __uint_as_float(o[8 * e + 5]) * invl),
+                       pack_bf16x2(__uint_as_float(o[8 * e + 6]) * invl, __uint_as_float(o[8 * e + 7]) * invl));
+        }
+      } else {  // 8 units of 4 fp32; one box per chunk of the pass
+        const uint32_t base = row + (k & 7) * OBOX;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          st_shared_v4(base + ((static_cast<uint32_t>(e) ^ sw) << 4),
+                       __float_as_uint(__uint_as_float(o[4 * e + 0]) * invl),
+                       __float_as_uint(__uint_as_float(o[4 * e + 1]) * invl),
+                       __float_as_uint(__uint_as_float(o[4 * e + 2]) * invl),
+                       __float_as_uint(__uint_as_float(o[4 * e + 3]) * invl));
+      }
+    }
+    // the box is complete for this row: bf16 after its second chunk, fp32 after each chunk
+    if (!no_split || (k & 1) == 1) {
+      fence_proxy_async_smem();
+      mbar_arrive(c.bar(B_OSTAGE + (no_split ? (k >> 1) : (k & 7))));
+    }
+  };
+  for (int pass = 0; pass < passes; ++pass) {
+    if (pass > 0 && !c.wait_warp(B_OFREE, 0)) return false;
+    const int c0 = no_split ? 0 : pass * 8, c1 = no_split ? 16 : c0 + 8;
+    uint32_t oa[32], ob[32];
+    tmem_ld16(to + c0 * 32, oa);
+    tmem_ld16(to + c0 * 32 + 16, oa + 16);
+#pragma unroll 1
+    for (int k = c0; k < c1; k += 2) {
+      tmem_wait_ld();
+      tmem_ld16(to + (k + 1) * 32, ob);
+      tmem_ld16(to + (k + 1) * 32 + 16, ob + 16);
+      stage_chunk(oa, k);
+      tmem_wait_ld();
+      if (k + 2 < c1) {
+        tmem_ld16(to + (k + 2) * 32, oa);
+        tmem_ld16(to + (k + 2) * 32 + 16, oa + 16);
+      }
+      stage_chunk(ob, k + 1);
+    }
+  }
+  return true;
+}
+
+// O-CTA store issuer (one lane of an otherwise idle warp): for the partition's last range,
+// sends each staged output box with a tiled TMA store as soon as all its rows are in, and
+// waits for the stores before the CTA may leave.
+__device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Plan& pl, int s) {
+  const int req = pl.end_req;
+  const int first_slot = p.nsplits[req];
+  const bool no_split = p.nsplits[req + 1] - first_slot == 1;
+  const int split = req == pl.begin_req ? pl.begin_split : first_slot;
+  const int row0 = no_split ? (req * p.s_q + s) * p.h_q : (split * p.s_q + s) * p.h_q;
+  const uint32_t stage = c.sbase + OFF_TILE;
+  const void* map = no_split ? static_cast<const void*>(&p.out_map)
+                             : static_cast<const void*>(&p.acc_map);
+  const int passes = no_split ? 1 : 2;
+  bool ok = true;
+  for (int pass = 0; pass < passes && ok; ++pass) {
+    for (int box = 0; box < 8; ++box) {
+      if (!c.wait(B_OSTAGE + box, static_cast<uint32_t>(pass) & 1u)) {
+        ok = false;
+        break;
+      }
+      tma_store_2d(map, no_split ? box * 64 : (pass * 8 + box) * 32, row0, stage + box * OBOX);
+      bulk_commit_group();
+    }
+    if (ok && pass + 1 < passes) {
+      bulk_wait_read_all();  // the staging tiles may be written again
+      mbar_arrive(c.bar(B_OFREE));
+    }
+  }
+  bulk_wait_all();  // every issued store is complete before this CTA can leave
+}
+
+// ---------------------------------------------------------------------------------------
 // O-CTA correction + epilogue warpgroup: thread i owns O row i.
 __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const Plan& pl, int s,
                                      uint32_t tbase, int i) {
@@ -596,43 +755,10 @@ __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const 
     const bool no_split = p.nsplits[req + 1] - first_slot == 1;
     const int split = req == pl.begin_req ? pl.begin_split : first_slot;
     const int tok = req * p.s_q + s;
-    if (no_split) {
-      __nv_bfloat16* dst = p.out + (static_cast<size_t>(tok) * p.h_q + (live ? i : 0)) * kDV;
-#pragma unroll 1
-      for (int k = 0; k < 512; k += 32) {
-        uint32_t o[32];
-        tmem_ld16(to + k, o);
-        tmem_ld16(to + k + 16, o + 16);
-        tmem_wait_ld();
-        if (live) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + k);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * invl, __uint_as_float(o[8 * e + 1]) * invl);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * invl, __uint_as_float(o[8 * e + 3]) * invl);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * invl, __uint_as_float(o[8 * e + 5]) * invl);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * invl, __uint_as_float(o[8 * e + 7]) * invl);
-            d4[e] = v;
-          }
-        }
-      }
-    } else {
-      float* dst = p.o_accum + ((static_cast<size_t>(split) * p.s_q + s) * p.h_q + (live ? i : 0)) * kDV;
-#pragma unroll 1
-      for (int k = 0; k < 512; k += 32) {
-        uint32_t o[32];
-        tmem_ld16(to + k, o);
-        tmem_ld16(to + k + 16, o + 16);
-        tmem_wait_ld();
-        if (live) {
-          float4* d4 = reinterpret_cast<float4*>(dst + k);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            d4[e] = make_float4(__uint_as_float(o[4 * e]) * invl, __uint_as_float(o[4 * e + 1]) * invl,
-                                __uint_as_float(o[4 * e + 2]) * invl, __uint_as_float(o[4 * e + 3]) * invl);
-        }
-      }
+    if (req == pl.end_req) {  // the value tiles are free now: stage O there for TMA stores
+      if (!drain_o_tma(p, c, to, i, no_split, invl)) return;
+    } else {  // the dequant warps are already filling the tiles for the next range
+      drain_o(p, to, i, no_split, split, tok, s, invl, 0, 16);
     }
     tc_fence_before();
     mbar_arrive(c.bar(B_O_EMPTY));
@@ -691,6 +817,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     mbar_init(c.bar(B_Q_FULL), 128);
     mbar_init(c.bar(B_QLOAD), 1);
     mbar_init(c.bar(B_QREAD), 128);
+    for (int b = 0; b < 8; ++b) mbar_init(c.bar(B_OSTAGE + b), 128);
+    mbar_init(c.bar(B_OFREE), 1);
     mbar_init(c.bar(B_O_FULL), 1);
     mbar_init(c.bar(B_O_EMPTY), 128);
     mbar_init(c.bar(B_DRAIN), 1);
@@ -736,7 +864,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
     } else if (warp == 8) {
       if (!scores && lane == 0) role_relay(c, pl);
+    } else if (warp == 4) {
+      if (!scores && lane == 0) role_store_issuer(p, c, pl, s);
     }
+
   }
   tc_fence_before();
   __syncthreads();

@@ -48,7 +48,11 @@ inline AccumLayout accum_layout(int b, int s_q, int h_q, int parts) {
 struct DecodeParams {
   // Q as a 2-D tensor (rows = token * h_q + head, 576 bf16 columns), box 64 columns x h_q rows,
   // 128-byte swizzle: one box is one 64-dim chunk of a token's Q in the SW128 K-major layout.
-  CUtensorMap q_map;  // (the type is 64-byte aligned)
+  CUtensorMap q_map;    // (the type is 64-byte aligned)
+  // out as rows (token * h_q + head) x 512 bf16, box 64 columns x h_q rows, 128-byte swizzle
+  CUtensorMap out_map;
+  // o_accum as rows ((split * s_q + s) * h_q + head) x 512 fp32, box 32 columns x h_q rows
+  CUtensorMap acc_map;
   const __nv_bfloat16* q;   // [b][s_q][h_q][576]
   const uint8_t* kv;        // [num_rows][656]
   const int32_t* indices;   // [b][s_q][topk]
@@ -62,6 +66,7 @@ struct DecodeParams {
   int b, s_q, h_q, topk;
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
+  int store32;              // out and the workspace are 32-byte aligned (256-bit stores)
 };
 
 struct CombineParams {
@@ -73,8 +78,10 @@ struct CombineParams {
   int b, s_q, h_q;
 };
 
-// Encodes DecodeParams::q_map for q (host; false if the driver call is missing or fails).
-bool encode_q_map(CUtensorMap* map, const void* q, int64_t tokens, int h_q);
+// Encodes a 2-D row-major tensor map (rows x cols, 128-byte swizzle, box box_cols x box_rows)
+// (host; false if the driver call is missing or fails).
+bool encode_rows_map(CUtensorMap* map, const void* base, bool fp32, int64_t rows, int cols,
+                     int box_cols, int box_rows);
 
 // Kernel launchers (return the launch's cudaError_t).
 cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int32_t* prefix,
