@@ -119,13 +119,6 @@ __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int
     }
     __syncwarp();
   }
-  // The plan buffer may still be read by the kernels of the previous decode on this stream:
-  // write nothing before they are done (this launch may start early).
-  griddep_wait();
-  if (lane == 0) {
-    status[0] = 0u;
-    status[1] = 0u;
-  }
   int first = 0;  // first partition taken by the exact walk below
   int ns = 0;
   if (levels >= 0) {
@@ -199,6 +192,14 @@ __global__ void __launch_bounds__(32) sched_kernel(int b, int s_q, int topk, int
     n_starts = ns;
   }
   __syncwarp();
+  // The plan is computed in shared memory from the shapes alone; the plan buffer may still be
+  // read by the kernels of the previous decode on this stream, so nothing is written to global
+  // memory before they are done (this launch may start early).
+  griddep_wait();
+  if (lane == 0) {
+    status[0] = 0u;
+    status[1] = 0u;
+  }
   const int4* src = reinterpret_cast<const int4*>(smeta);
   int4* dst = reinterpret_cast<int4*>(meta);
   for (int i = lane; i < parts * (kMetaInts / 4); i += 32) dst[i] = src[i];
