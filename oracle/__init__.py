@@ -10,6 +10,7 @@ code, header, table or constant.
 * ``sched.py`` -- the greedy split-KV partition planner.
 * ``combine.py`` -- the LSE-weighted merge of split partials.
 * ``online.py`` -- the base-2 online softmax recurrence, step by step.
+* ``variants.py`` -- per-token top-k length masking and the attention-sink output factor.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle*.py`` (worked-example values from the pages, closed forms, brute force
@@ -25,7 +26,7 @@ import threading
 
 import numpy as np
 
-from . import combine, online, sched  # noqa: F401  (re-exported)
+from . import combine, online, sched, variants  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "sparse_mla_oracle.c")
@@ -105,7 +106,8 @@ def decode_row(row: np.ndarray) -> np.ndarray:
 
 
 def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, sm_scale: float,
-                      tokens=None, slot_range=None, threads: int = 0):
+                      tokens=None, slot_range=None, threads: int = 0, attn_sink=None,
+                      topk_length=None):
     """Sparse MLA decode in fp64.
 
     q_bits:  uint16 bf16 bit patterns [b, s_q, h_q, 576]
@@ -113,6 +115,8 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
     indices: int32 [b, s_q, topk]
     tokens:  optional list of flattened query-token ids (bi * s_q + si); default all
     slot_range: optional (begin, end) sub-range of the top-k slots (one split's share)
+    attn_sink:   optional per-head sink values [h_q] (``variants``); whole rows only
+    topk_length: optional per-token valid prefix lengths [b, s_q] (``variants``)
 
     Returns (out fp64 [n_tok, h_q, 512], lse fp64 [n_tok, h_q], n_valid int32 [n_tok])
     where n_tok runs over ``tokens`` in order.
@@ -123,6 +127,8 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
     kv = np.ascontiguousarray(kv, dtype=np.uint8)
     assert kv.shape[-1] == ROW_BYTES
     num_blocks, page = kv.shape[0], kv.shape[1]
+    if topk_length is not None:
+        indices = variants.mask_beyond_length(indices, topk_length)
     indices = np.ascontiguousarray(indices, dtype=np.int32)
     assert indices.shape[:2] == (b, s_q)
     topk = indices.shape[2]
@@ -140,12 +146,18 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
                                            _ptr(lse), _ptr(nv), int(threads))
     if rc != 0:
         raise MemoryError("oracle allocation failed")
+    if attn_sink is not None:
+        assert slot_range is None, "the sink scales whole rows, not one split's share"
+        sink = np.asarray(attn_sink, dtype=np.float64).reshape(1, h_q)
+        out *= variants.sink_factor(lse, sink)[:, :, None]
     return out, lse, nv
 
 
-def sparse_mla_decode_full(q_bits, kv, indices, sm_scale, threads: int = 0):
+def sparse_mla_decode_full(q_bits, kv, indices, sm_scale, threads: int = 0, attn_sink=None,
+                           topk_length=None):
     """Whole-problem form with the library's output layouts: out [b, s_q, h_q, 512],
     lse [b, h_q, s_q]."""
     b, s_q, h_q, _ = q_bits.shape
-    out, lse, _ = sparse_mla_decode(q_bits, kv, indices, sm_scale, threads=threads)
+    out, lse, _ = sparse_mla_decode(q_bits, kv, indices, sm_scale, threads=threads,
+                                    attn_sink=attn_sink, topk_length=topk_length)
     return out.reshape(b, s_q, h_q, D_V), lse.reshape(b, s_q, h_q).transpose(0, 2, 1).copy()

@@ -19,11 +19,14 @@ import math
 import numpy as np
 
 
-def combine(lse2: np.ndarray, o: np.ndarray) -> tuple[np.ndarray, float]:
+def combine(lse2: np.ndarray, o: np.ndarray, attn_sink=None) -> tuple[np.ndarray, float]:
     """Merge splits for one (token, head).
 
     lse2: [n_splits] base-2 log-sum-exp of each split (-inf for an empty split).
     o:    [n_splits, d_v] each split's output, already divided by its own exp-sum.
+    attn_sink: optional sink value of this head: the merged output is then multiplied by
+          1 / (1 + exp(attn_sink - lse)) with the merged lse ("FlashMLA 与 DSA", section
+          4.3); the lse itself is returned unchanged.
     Returns (merged output [d_v], merged natural-log lse).
     """
     lse2 = np.asarray(lse2, dtype=np.float64)
@@ -34,7 +37,11 @@ def combine(lse2: np.ndarray, o: np.ndarray) -> tuple[np.ndarray, float]:
     w = np.exp2(lse2 - m)
     total = float(np.sum(w))
     merged = (w[:, None] * o).sum(axis=0) / total
-    return merged, (m + math.log2(total)) * math.log(2.0)
+    lse = (m + math.log2(total)) * math.log(2.0)
+    if attn_sink is not None:
+        with np.errstate(over="ignore"):
+            merged = merged / (1.0 + np.exp(np.float64(attn_sink) - lse))
+    return merged, lse
 
 
 def weights(lse2: np.ndarray) -> np.ndarray:

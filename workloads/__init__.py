@@ -206,6 +206,30 @@ def small(b=2, s_q=1, h_q=128, topk=128, ctx=512, ue8m0=False, masked_per_row=0,
     return make(spec, device=device)
 
 
+def attn_sink(h_q: int, seed: int, device="cpu") -> torch.Tensor:
+    """fp32 [h_q] per-head sink values: head 0 takes -2.5 (the worked example's value), the
+    others are uniform on [-4, 10], a range that straddles the log-sum-exp of a few hundred
+    to a few thousand keys with unit-variance scores, so the sink visibly changes some rows
+    and barely touches others."""
+    g = _gen(torch.device("cpu"), seed)
+    s = torch.rand(h_q, generator=g, dtype=torch.float64) * 14.0 - 4.0
+    s[0] = -2.5
+    return s.float().to(device)
+
+
+def topk_lengths(b: int, s_q: int, topk: int, seed: int, device="cpu") -> torch.Tensor:
+    """int32 [b, s_q] per-token valid prefix lengths: uniform on [0, topk], with the edge
+    values 0, 1, 63, 64, 65, topk and topk + 7 (beyond the list) placed on the first tokens
+    when they fit."""
+    g = _gen(torch.device("cpu"), seed)
+    n = b * s_q
+    lens = torch.randint(0, topk + 1, (n,), generator=g, dtype=torch.int64)
+    edges = [v for v in (0, 1, 63, 64, 65, topk, topk + 7) if v <= topk + 7]
+    k = min(n, len(edges))
+    lens[:k] = torch.tensor(edges[:k], dtype=torch.int64)
+    return lens.to(torch.int32).view(b, s_q).to(device)
+
+
 def to_numpy_inputs(wl: Workload):
     """(q as uint16 bf16 bits, kv uint8, indices int32) numpy arrays on the host."""
     q = wl.q.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
