@@ -147,6 +147,47 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
                                float* lse, void* stream);
 
 /*
+ * Optional inputs of the decode variants ("FlashMLA 与 DSA：内核、流水线和正确性边界",
+ * section 4.3, the reference semantics; "FlashMLA Sparse Decode 完整计算过程详解", step 13,
+ * the attention sink inside the kernel).  A NULL field leaves its variant off; a NULL
+ * smla_decode_opts pointer leaves all of them off.
+ *   attn_sink    device fp32 [h_q], 4-byte aligned: one sink score per query head.  The
+ *                output row becomes out * 1 / (1 + exp(attn_sink[h] - lse)): the sink acts
+ *                as one more key with score attn_sink[h] and a zero value vector.  The
+ *                returned lse is that of the real slots only (unchanged by the sink).  A row
+ *                with no valid slot keeps out = 0, lse = +inf.
+ *   topk_length  device int32 [b][s_q], 4-byte aligned: slot j of token t is masked when
+ *                j >= topk_length[t], in addition to the index rule; a length above topk
+ *                keeps every slot, a length <= 0 masks the whole row.  The plan still
+ *                covers all topk slots (masked slots cost no cache reads, but their blocks
+ *                still pass through the pipeline).
+ * The same options must be given to sparse_mla_decode_fwd_ex and sparse_mla_combine_ex of
+ * one problem: the decode pass applies the sink to unsplit rows, the combine to split rows.
+ */
+typedef struct {
+  const float* attn_sink;
+  const int32_t* topk_length;
+} smla_decode_opts;
+
+/* sparse_mla_decode_fwd with decode options (opts may be NULL: then identical to it).
+ * Errors: as sparse_mla_decode_fwd; SMLA_ERR_ALIGNMENT for a misaligned option pointer. */
+smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const void* q,
+                                     const void* kv_cache, const int32_t* indices,
+                                     float sm_scale, const smla_decode_opts* opts,
+                                     const void* sched_meta, void* workspace,
+                                     size_t workspace_bytes, void* out, float* lse,
+                                     void* stream);
+
+/* sparse_mla_combine with decode options (opts may be NULL: then identical to it).  With
+ * attn_sink set, a split row's merged output is divided by sum_j w_j + 2^(attn_sink[h]
+ * log2(e) - M) instead of sum_j w_j (the same factor as above); topk_length is not read
+ * here.  Errors: as sparse_mla_combine. */
+smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
+                                  const smla_decode_opts* opts, const void* sched_meta,
+                                  const void* workspace, size_t workspace_bytes, void* out,
+                                  float* lse, void* stream);
+
+/*
  * sparse_mla_decode_static -- sparse_mla_sched_meta, sparse_mla_decode_fwd and
  * sparse_mla_combine in one call, on scratch memory owned by the library instead of the
  * caller.  The pages describe no such call: it exists for callers that cannot provide

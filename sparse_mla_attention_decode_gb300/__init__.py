@@ -20,6 +20,7 @@ __all__ = [
     "sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
     "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
     "sparse_mla_version", "sparse_mla_decode_static", "STATIC_SCRATCH_BYTES",
+    "smla_decode_opts", "sparse_mla_decode_fwd_ex", "sparse_mla_combine_ex",
     "SparseMLADecode", "dims_for",
 ]
 
@@ -34,7 +35,8 @@ SMLA_ERR_TIMEOUT = 6
 SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
-            "sparse_mla_version", "sparse_mla_decode_static"]
+            "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
+            "sparse_mla_combine_ex"]
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -49,6 +51,12 @@ class smla_dims(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int32), ("s_q", ctypes.c_int32), ("h_q", ctypes.c_int32),
                 ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("page_block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64)]
+
+
+class smla_decode_opts(ctypes.Structure):
+    """Optional decode inputs: device pointers (0 = variant off) to fp32 attn_sink [h_q] and
+    int32 topk_length [b, s_q]."""
+    _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -77,6 +85,11 @@ def lib():
             L.sparse_mla_decode_fwd.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, vp,
                                                 ctypes.c_float, vp, vp, sz, vp, vp, vp]
             L.sparse_mla_combine.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, sz, vp, vp, vp]
+            L.sparse_mla_decode_fwd_ex.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, vp,
+                                                   ctypes.c_float, P(smla_decode_opts), vp, vp,
+                                                   sz, vp, vp, vp]
+            L.sparse_mla_combine_ex.argtypes = [P(smla_dims), ctypes.c_int, P(smla_decode_opts),
+                                                vp, vp, sz, vp, vp, vp]
             L.sparse_mla_status_string.argtypes = [ctypes.c_int]
             L.sparse_mla_status_string.restype = ctypes.c_char_p
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
@@ -133,6 +146,25 @@ def sparse_mla_combine(dims: smla_dims, num_sms: int, sched_meta: int, workspace
            "sparse_mla_combine")
 
 
+def sparse_mla_decode_fwd_ex(dims: smla_dims, num_sms: int, q: int, kv_cache: int, indices: int,
+                             sm_scale: float, opts, sched_meta: int, workspace: int,
+                             workspace_bytes: int, out: int, lse: int, stream: int = 0) -> None:
+    _check(lib().sparse_mla_decode_fwd_ex(ctypes.byref(dims), int(num_sms), q, kv_cache, indices,
+                                          float(sm_scale),
+                                          None if opts is None else ctypes.byref(opts),
+                                          sched_meta, workspace, int(workspace_bytes), out, lse,
+                                          stream),
+           "sparse_mla_decode_fwd_ex")
+
+
+def sparse_mla_combine_ex(dims: smla_dims, num_sms: int, opts, sched_meta: int, workspace: int,
+                          workspace_bytes: int, out: int, lse: int, stream: int = 0) -> None:
+    _check(lib().sparse_mla_combine_ex(ctypes.byref(dims), int(num_sms),
+                                       None if opts is None else ctypes.byref(opts), sched_meta,
+                                       workspace, int(workspace_bytes), out, lse, stream),
+           "sparse_mla_combine_ex")
+
+
 def sparse_mla_decode_static(dims: smla_dims, num_sms: int, q: int, kv_cache: int,
                              indices: int, sm_scale: float, out: int, lse: int,
                              stream: int = 0) -> None:
@@ -170,6 +202,8 @@ class SparseMLADecode:
 
     q: bf16 [b, s_q, h_q, 576]; kv_cache: uint8 [num_blocks, 64, 1, 656]; indices: int32
     [b, s_q, topk]; returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, h_q, s_q]).
+    Optional ``attn_sink`` (fp32 [h_q]) and ``topk_length`` (int32 [b, s_q]) device tensors
+    select the decode variants of ``smla_decode_opts``.
     """
 
     def __init__(self, b: int, s_q: int, h_q: int, topk: int, num_blocks: int, device=None,
@@ -185,7 +219,8 @@ class SparseMLADecode:
         self.sched = torch.empty(max(sb, 16), dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(max(ab, 16), dtype=torch.uint8, device=self.device)
 
-    def run(self, q, kv_cache, indices, sm_scale: float, out=None, lse=None, stream=None):
+    def run(self, q, kv_cache, indices, sm_scale: float, out=None, lse=None, stream=None,
+            attn_sink=None, topk_length=None):
         import torch
         d = self.dims
         if out is None:
@@ -197,13 +232,26 @@ class SparseMLADecode:
                         ("lse", lse)):
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
+        opts = None
+        if attn_sink is not None or topk_length is not None:
+            if attn_sink is not None and (attn_sink.dtype != torch.float32
+                                          or attn_sink.numel() != d.h_q
+                                          or not attn_sink.is_contiguous()):
+                raise ValueError("attn_sink must be a contiguous fp32 tensor of h_q values")
+            if topk_length is not None and (topk_length.dtype != torch.int32
+                                            or topk_length.numel() != d.b * d.s_q
+                                            or not topk_length.is_contiguous()):
+                raise ValueError("topk_length must be a contiguous int32 tensor [b, s_q]")
+            opts = smla_decode_opts(attn_sink.data_ptr() if attn_sink is not None else None,
+                                    topk_length.data_ptr() if topk_length is not None else None)
         sparse_mla_sched_meta(d, self.num_sms, self.sched.data_ptr(), self.sched_bytes, st)
-        sparse_mla_decode_fwd(d, self.num_sms, q.data_ptr(), kv_cache.data_ptr(),
-                              indices.data_ptr(), sm_scale, self.sched.data_ptr(),
+        sparse_mla_decode_fwd_ex(d, self.num_sms, q.data_ptr(), kv_cache.data_ptr(),
+                                 indices.data_ptr(), sm_scale, opts, self.sched.data_ptr(),
+                                 self.workspace.data_ptr(), self.accum_bytes, out.data_ptr(),
+                                 lse.data_ptr(), st)
+        sparse_mla_combine_ex(d, self.num_sms, opts, self.sched.data_ptr(),
                               self.workspace.data_ptr(), self.accum_bytes, out.data_ptr(),
                               lse.data_ptr(), st)
-        sparse_mla_combine(d, self.num_sms, self.sched.data_ptr(), self.workspace.data_ptr(),
-                           self.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
         return out, lse
 
     def device_status(self, stream=None) -> int:

@@ -27,6 +27,13 @@ smla_status check_dims(const smla_dims* d) {
   return SMLA_OK;
 }
 
+// Option pointers are optional; those given must be 4-byte aligned (fp32 / int32 arrays).
+smla_status check_opts(const smla_decode_opts* o) {
+  if (o == nullptr) return SMLA_OK;
+  if (!aligned(o->attn_sink, 4) || !aligned(o->topk_length, 4)) return SMLA_ERR_ALIGNMENT;
+  return SMLA_OK;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -140,6 +147,16 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
                                   const void* kv_cache, const int32_t* indices, float sm_scale,
                                   const void* sched_meta, void* workspace, size_t workspace_bytes,
                                   void* out, float* lse, void* stream) {
+  return sparse_mla_decode_fwd_ex(dims, num_sms, q, kv_cache, indices, sm_scale, nullptr,
+                                  sched_meta, workspace, workspace_bytes, out, lse, stream);
+}
+
+smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const void* q,
+                                     const void* kv_cache, const int32_t* indices,
+                                     float sm_scale, const smla_decode_opts* opts,
+                                     const void* sched_meta, void* workspace,
+                                     size_t workspace_bytes, void* out, float* lse,
+                                     void* stream) {
   smla_status st = check_dims(dims);
   if (st != SMLA_OK) return st;
   const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
@@ -150,6 +167,7 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 16) ||
       !aligned(sched_meta, 16) || !aligned(indices, 4) || !aligned(lse, 4))
     return SMLA_ERR_ALIGNMENT;
+  if ((st = check_opts(opts)) != SMLA_OK) return st;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
   const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
@@ -177,6 +195,8 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
   p.meta = reinterpret_cast<const int32_t*>(plan + L.meta_off);
   p.nsplits = reinterpret_cast<const int32_t*>(plan + L.prefix_off);
   p.status = const_cast<uint32_t*>(reinterpret_cast<const uint32_t*>(plan + L.status_off));
+  p.attn_sink = opts != nullptr ? opts->attn_sink : nullptr;
+  p.topk_length = opts != nullptr ? opts->topk_length : nullptr;
   p.b = dims->b;
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;
@@ -190,6 +210,14 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
 smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* sched_meta,
                                const void* workspace, size_t workspace_bytes, void* out, float* lse,
                                void* stream) {
+  return sparse_mla_combine_ex(dims, num_sms, nullptr, sched_meta, workspace, workspace_bytes,
+                               out, lse, stream);
+}
+
+smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
+                                  const smla_decode_opts* opts, const void* sched_meta,
+                                  const void* workspace, size_t workspace_bytes, void* out,
+                                  float* lse, void* stream) {
   smla_status st = check_dims(dims);
   if (st != SMLA_OK) return st;
   const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
@@ -197,6 +225,7 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
   if (!sched_meta || !workspace || !out || !lse) return SMLA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(workspace, 16) || !aligned(sched_meta, 16) || !aligned(lse, 4))
     return SMLA_ERR_ALIGNMENT;
+  if ((st = check_opts(opts)) != SMLA_OK) return st;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
   const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
@@ -208,6 +237,7 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
   p.nsplits = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(sched_meta) + L.prefix_off);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.attn_sink = opts != nullptr ? opts->attn_sink : nullptr;
   p.b = dims->b;
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;

@@ -197,11 +197,16 @@ struct RowCopy {
 };
 static_assert(8 * RING * RowCopy<true>::kBytes <= RAW_BYTES, "row ring");
 
+// Index of one slot, -1 for a slot past the list or past the token's topk_length (both
+// loads are issued before either is tested).
 __device__ __forceinline__ int32_t load_index(const DecodeParams& p, int s, int req, int blk,
                                               int row) {
   const int slot = blk * BT + row;
   if (slot >= p.topk) return -1;
-  return ldg_s32(p.indices + (static_cast<size_t>(req) * p.s_q + s) * p.topk + slot);
+  const size_t tok = static_cast<size_t>(req) * p.s_q + s;
+  const int32_t ix = ldg_s32(p.indices + tok * p.topk + slot);
+  if (p.topk_length != nullptr && slot >= ldg_s32(p.topk_length + tok)) return -1;
+  return ix;
 }
 
 // Copies this lane's share of one row (j = lane % 8) into its ring slot; one commit group per
@@ -524,11 +529,16 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       l = l * alpha + sum;
       st_shared_f32(msg + MSG_ALPHA + 4 * i, alpha);
       if (blk == b1 - 1) {
-        // last block of the range: the O-CTA's normalisation, and the lse from here
-        st_shared_f32(msg + MSG_INVL + 4 * i, l == 0.f ? 0.f : 1.f / (l * 256.f));
+        // last block of the range: the O-CTA's normalisation, and the lse from here.  An
+        // unsplit row with an attention sink divides by L + 2^(sink log2(e) - m) instead of
+        // L (the sink as one more key with a zero value; split rows get it in the combine).
+        const int first_slot = p.nsplits[req];
+        const bool no_split = p.nsplits[req + 1] - first_slot == 1;
+        float denom = l;
+        if (no_split && live && p.attn_sink != nullptr && l != 0.f)
+          denom += ex2(fmaf(__ldg(p.attn_sink + i), 1.4426950408889634f, -m));
+        st_shared_f32(msg + MSG_INVL + 4 * i, l == 0.f ? 0.f : 1.f / (denom * 256.f));
         if (live) {
-          const int first_slot = p.nsplits[req];
-          const bool no_split = p.nsplits[req + 1] - first_slot == 1;
           if (no_split) {
             p.lse[(static_cast<size_t>(req) * p.h_q + i) * p.s_q + s] =
                 l == 0.f ? INFINITY : (log2f(l) + m) * 0.69314718055994530942f;

@@ -293,7 +293,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
       acc[c].x += w * v.x; acc[c].y += w * v.y; acc[c].z += w * v.z; acc[c].w += w * v.w;
     }
   }
-  const float inv = 1.f / wsum;
+  // an attention sink adds one zero-value key of score attn_sink[h] to the merged row
+  const float sink = p.attn_sink != nullptr
+                         ? exp2f(fmaf(__ldg(p.attn_sink + h), 1.4426950408889634f, -mx))
+                         : 0.f;
+  const float inv = 1.f / (wsum + sink);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint2 pk;

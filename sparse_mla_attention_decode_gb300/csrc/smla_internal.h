@@ -63,6 +63,8 @@ struct DecodeParams {
   const int32_t* meta;      // [parts][8]
   const int32_t* nsplits;   // [b + 1]
   uint32_t* status;         // device status word
+  const float* attn_sink;   // [h_q] or null
+  const int32_t* topk_length;  // [b][s_q] or null
   int b, s_q, h_q, topk;
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
@@ -75,6 +77,7 @@ struct CombineParams {
   const int32_t* nsplits;
   __nv_bfloat16* out;
   float* lse;
+  const float* attn_sink;  // [h_q] or null
   int b, s_q, h_q;
 };
 

@@ -16,11 +16,13 @@ O_REL_L2 = 5e-3
 LSE_ABS = 1e-3
 
 
-def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True):
+def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True,
+             attn_sink=None, topk_length=None):
     dev = wl.q.device
     op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
                               wl.kv.shape[0], device=dev, num_sms=num_sms)
-    out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale)
+    out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale, attn_sink=attn_sink,
+                      topk_length=topk_length)
     torch.cuda.synchronize(dev)
     if check_status:
         word = op.device_status()
@@ -51,11 +53,18 @@ def compact_inputs(wl: workloads.Workload, tokens: np.ndarray):
     return qb, kvn, idn
 
 
-def oracle_tokens(wl: workloads.Workload, tokens, threads: int = 0):
-    """Oracle (out [n, h, 512], lse [n, h]) for the given flattened query tokens."""
+def oracle_tokens(wl: workloads.Workload, tokens, threads: int = 0, attn_sink=None,
+                  topk_length=None):
+    """Oracle (out [n, h, 512], lse [n, h]) for the given flattened query tokens, with the
+    optional decode variants (sink [h_q], per-token lengths [b, s_q]) as host tensors."""
     tokens = np.asarray(tokens, dtype=np.int64)
     qb, kvn, idn = compact_inputs(wl, tokens)
-    out, lse, _ = oracle.sparse_mla_decode(qb, kvn, idn, wl.sm_scale, threads=threads)
+    sink = None if attn_sink is None else attn_sink.double().cpu().numpy()
+    lens = None
+    if topk_length is not None:
+        lens = topk_length.reshape(-1).cpu().numpy()[tokens].reshape(-1, 1)
+    out, lse, _ = oracle.sparse_mla_decode(qb, kvn, idn, wl.sm_scale, threads=threads,
+                                           attn_sink=sink, topk_length=lens)
     return out, lse
 
 

@@ -90,6 +90,32 @@ def test_pointer_checks_before_launch(L):
     assert L.sparse_mla_read_device_status(ctypes.byref(d), 152, None, ctypes.byref(code), None) == 1
 
 
+def test_decode_option_checks_before_launch(L):
+    d = smla.dims_for(2, 1, 128, 128, 64)
+    sb, ab = smla.sparse_mla_workspace_size(d, 152)
+    fake = 0x10000
+
+    def fwd(opts):
+        return L.sparse_mla_decode_fwd_ex(ctypes.byref(d), 152, fake, fake, fake,
+                                          ctypes.c_float(0.0417), opts, fake, fake, ab, fake,
+                                          fake, None)
+
+    def comb(opts):
+        return L.sparse_mla_combine_ex(ctypes.byref(d), 152, opts, fake, fake, ab, fake, fake,
+                                       None)
+
+    for bad in (smla.smla_decode_opts(fake + 2, None), smla.smla_decode_opts(None, fake + 1)):
+        assert fwd(ctypes.byref(bad)) == 3
+        assert comb(ctypes.byref(bad)) == 3
+    # other argument errors still come first or alongside: a null q with options set
+    ok = smla.smla_decode_opts(fake, fake)
+    assert L.sparse_mla_decode_fwd_ex(ctypes.byref(d), 152, None, fake, fake,
+                                      ctypes.c_float(0.0417), ctypes.byref(ok), fake, fake, ab,
+                                      fake, fake, None) == 1
+    assert L.sparse_mla_combine_ex(ctypes.byref(d), 152, ctypes.byref(ok), fake, fake, ab - 1,
+                                   fake, fake, None) == 4
+
+
 def test_no_device_is_a_cuda_error_not_a_crash(L):
     import torch
     if torch.cuda.is_available():

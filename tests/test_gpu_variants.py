@@ -1,0 +1,135 @@
+"""GPU parity of the decode variants (attention sink, per-token top-k length) through the C
+ABI against the fp64 oracle: small cases in full on unsplit and split plans, the combine
+kernel with a sink on synthetic partials, and the full-size b=64 / h=128 / topk=2048
+workload with both variants on sampled tokens."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import sparse_mla_attention_decode_gb300 as smla
+    smla.lib()
+    return torch.device("cuda:0")
+
+
+def _full(wl, num_sms, what, sink=None, lens=None):
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, topk_length=lens)
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    ro, rl = oracle.sparse_mla_decode_full(
+        q, kv, idx, wl.sm_scale,
+        attn_sink=None if sink is None else sink.double().cpu().numpy(),
+        topk_length=None if lens is None else lens.cpu().numpy())
+    h = wl.spec.h_q
+    go = out.double().cpu().numpy().reshape(-1, h, 512)
+    gl = lse.double().cpu().numpy().transpose(0, 2, 1).reshape(-1, h)
+    m = gu.compare(go, gl, ro.reshape(-1, h, 512), rl.transpose(0, 2, 1).reshape(-1, h), what)
+    return m, go
+
+
+CASES = [
+    # (name, workload kwargs, num_sms, sink, lengths)
+    ("sink_nosplit_h128", dict(b=3, h_q=128, topk=300, ctx=2048, masked_per_row=20), 8,
+     True, False),
+    ("sink_split_h128", dict(b=3, h_q=128, topk=300, ctx=2048, masked_per_row=20), 132,
+     True, False),
+    ("sink_split_h64_sq2", dict(b=2, s_q=2, h_q=64, topk=256, ctx=1024, causal_base=700), 48,
+     True, False),
+    ("len_nosplit_h128", dict(b=7, h_q=128, topk=200, ctx=1024, masked_per_row=9), 8,
+     False, True),
+    ("len_split_h64", dict(b=4, s_q=2, h_q=64, topk=330, ctx=2048), 64, False, True),
+    ("both_split_h128", dict(b=7, h_q=128, topk=320, ctx=4096, ue8m0=True), 152, True, True),
+    ("both_nosplit_h64", dict(b=9, h_q=64, topk=130, ctx=1024, masked_per_row=5), 6,
+     True, True),
+]
+
+
+@pytest.mark.parametrize("name,kw,num_sms,use_sink,use_len", CASES, ids=[c[0] for c in CASES])
+def test_variant_parity(dev, name, kw, num_sms, use_sink, use_len):
+    seed = 500 + sum(map(ord, name))
+    wl = workloads.small(device=dev, seed=seed, **kw)
+    sink = workloads.attn_sink(wl.spec.h_q, seed, device=dev) if use_sink else None
+    lens = (workloads.topk_lengths(wl.spec.b, wl.spec.s_q, wl.spec.topk, seed, device=dev)
+            if use_len else None)
+    m, go = _full(wl, num_sms, name, sink, lens)
+    print(name, m)
+    # the variant must have changed the result: compare with the plain decode
+    plain, _, _ = gu.run_cuda(wl, num_sms=num_sms)
+    diff = np.abs(go - plain.double().cpu().numpy().reshape(go.shape)).max()
+    assert diff > 2 * gu.O_MAX_ABS, f"{name}: the variant left the output unchanged ({diff})"
+
+
+def test_combine_kernel_with_sink(dev):
+    import sparse_mla_attention_decode_gb300 as smla
+    from oracle import combine as ocomb
+    b, s_q, h = 3, 2, 64
+    op = smla.SparseMLADecode(b, s_q, h, 2048, 64, device=dev, num_sms=40)
+    st = torch.cuda.current_stream().cuda_stream
+    smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+    torch.cuda.synchronize()
+    _, pre = op.plan()
+    pre = pre.tolist()
+    parts = max(op.num_sms // s_q // 2, 1)
+    max_splits = b + parts
+    g = torch.Generator(device="cpu").manual_seed(14)
+    o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)
+    l_acc = torch.randn(max_splits, s_q, h, generator=g) * 4 + 6
+    l_acc[pre[1]:pre[2], 1, 7] = -math.inf  # a row whose splits are all empty
+    sink = workloads.attn_sink(h, 3)
+    sink[5] = 60.0   # far above every lse: output about 0
+    sink[6] = -60.0  # far below: no effect
+    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
+    ws = op.workspace
+    ws[: o_acc.numel() * 4].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
+    ws[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
+    out = torch.full((b, s_q, h, 512), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((b, h, s_q), 7.0, dtype=torch.float32, device=dev)
+    sink_d = sink.to(dev)
+    opts = smla.smla_decode_opts(sink_d.data_ptr(), None)
+    smla.sparse_mla_combine_ex(op.dims, op.num_sms, opts, op.sched.data_ptr(), ws.data_ptr(),
+                               op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+    torch.cuda.synchronize()
+    out, lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    checked = 0
+    for r in range(b):
+        n = pre[r + 1] - pre[r]
+        for s in range(s_q):
+            for hh in range(h):
+                if n <= 1:
+                    assert np.all(out[r, s, hh] == 7.0) and lse[r, hh, s] == 7.0
+                    continue
+                ro, rl = ocomb.combine(l_acc[pre[r]:pre[r + 1], s, hh].double().numpy(),
+                                       o_acc[pre[r]:pre[r + 1], s, hh].double().numpy(),
+                                       attn_sink=float(sink[hh]))
+                if math.isinf(rl):
+                    assert np.all(out[r, s, hh] == 0) and np.isposinf(lse[r, hh, s])
+                else:
+                    assert np.max(np.abs(out[r, s, hh] - ro)) <= 1e-2 * max(1, np.abs(ro).max())
+                    assert abs(lse[r, hh, s] - rl) <= 1e-4
+                    checked += 1
+    assert checked > 100
+
+
+def test_full_size_workload_with_variants(dev):
+    spec = workloads.CONFIGS["c2_b64_h128_k2048_mask5"]
+    wl = workloads.make(spec, device=dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sink = workloads.attn_sink(spec.h_q, 77, device=dev)
+    lens = workloads.topk_lengths(spec.b, spec.s_q, spec.topk, 77, device=dev)
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, topk_length=lens)
+    assert torch.isfinite(out.float()).all()
+    tokens = np.array(sorted(set([0, 1, 2, 3, 4, 5, 6, 63] +
+                                 list(np.random.default_rng(7).integers(0, 64, 12)))))
+    ro, rl = gu.oracle_tokens(wl, tokens, attn_sink=sink, topk_length=lens)
+    go, gl = gu.gpu_tokens(out, lse, wl, tokens)
+    print(gu.compare(go, gl, ro, rl, "c2 with sink and lengths"))
