@@ -161,12 +161,20 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
  *                keeps every slot, a length <= 0 masks the whole row.  The plan still
  *                covers all topk slots (masked slots cost no cache reads, but their blocks
  *                still pass through the pipeline).
+ *   partials_bf16  nonzero: the split partials of O go through the workspace as bf16
+ *                instead of fp32, halving their write and read traffic ("FlashMLA 与 DSA",
+ *                section 4.2 reports this trade for a split kernel: partials are already
+ *                normalised by their own exp-sum, so they are bounded by the largest value
+ *                element).  Results stay within the library's tolerance but differ in the
+ *                last bits from the fp32 path; the workspace size is unchanged.
  * The same options must be given to sparse_mla_decode_fwd_ex and sparse_mla_combine_ex of
- * one problem: the decode pass applies the sink to unsplit rows, the combine to split rows.
+ * one problem: the decode pass applies the sink to unsplit rows, the combine to split rows,
+ * and both must agree on the partials' type.
  */
 typedef struct {
   const float* attn_sink;
   const int32_t* topk_length;
+  int32_t partials_bf16;
 } smla_decode_opts;
 
 /* sparse_mla_decode_fwd with decode options (opts may be NULL: then identical to it).

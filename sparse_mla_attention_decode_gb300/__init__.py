@@ -55,8 +55,9 @@ class smla_dims(ctypes.Structure):
 
 class smla_decode_opts(ctypes.Structure):
     """Optional decode inputs: device pointers (0 = variant off) to fp32 attn_sink [h_q] and
-    int32 topk_length [b, s_q]."""
-    _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p)]
+    int32 topk_length [b, s_q]; partials_bf16 != 0 keeps split partials in bf16."""
+    _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p),
+                ("partials_bf16", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -203,7 +204,7 @@ class SparseMLADecode:
     q: bf16 [b, s_q, h_q, 576]; kv_cache: uint8 [num_blocks, 64, 1, 656]; indices: int32
     [b, s_q, topk]; returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, h_q, s_q]).
     Optional ``attn_sink`` (fp32 [h_q]) and ``topk_length`` (int32 [b, s_q]) device tensors
-    select the decode variants of ``smla_decode_opts``.
+    and ``partials_bf16`` select the decode variants of ``smla_decode_opts``.
     """
 
     def __init__(self, b: int, s_q: int, h_q: int, topk: int, num_blocks: int, device=None,
@@ -220,7 +221,7 @@ class SparseMLADecode:
         self.workspace = torch.empty(max(ab, 16), dtype=torch.uint8, device=self.device)
 
     def run(self, q, kv_cache, indices, sm_scale: float, out=None, lse=None, stream=None,
-            attn_sink=None, topk_length=None):
+            attn_sink=None, topk_length=None, partials_bf16: bool = False):
         import torch
         d = self.dims
         if out is None:
@@ -233,7 +234,7 @@ class SparseMLADecode:
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
         opts = None
-        if attn_sink is not None or topk_length is not None:
+        if attn_sink is not None or topk_length is not None or partials_bf16:
             if attn_sink is not None and (attn_sink.dtype != torch.float32
                                           or attn_sink.numel() != d.h_q
                                           or not attn_sink.is_contiguous()):
@@ -243,7 +244,8 @@ class SparseMLADecode:
                                             or not topk_length.is_contiguous()):
                 raise ValueError("topk_length must be a contiguous int32 tensor [b, s_q]")
             opts = smla_decode_opts(attn_sink.data_ptr() if attn_sink is not None else None,
-                                    topk_length.data_ptr() if topk_length is not None else None)
+                                    topk_length.data_ptr() if topk_length is not None else None,
+                                    1 if partials_bf16 else 0)
         sparse_mla_sched_meta(d, self.num_sms, self.sched.data_ptr(), self.sched_bytes, st)
         sparse_mla_decode_fwd_ex(d, self.num_sms, q.data_ptr(), kv_cache.data_ptr(),
                                  indices.data_ptr(), sm_scale, opts, self.sched.data_ptr(),

@@ -183,6 +183,9 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
       !encode_rows_map(&p.out_map, out, false, tokens * dims->h_q, kDV, 64, dims->h_q) ||
       !encode_rows_map(&p.acc_map, static_cast<uint8_t*>(workspace) + A.o_off, true,
                        static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q, kDV, 32,
+                       dims->h_q) ||
+      !encode_rows_map(&p.acc16_map, static_cast<uint8_t*>(workspace) + A.o_off, false,
+                       static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q, kDV, 64,
                        dims->h_q))
     return SMLA_ERR_CUDA;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -197,6 +200,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.status = const_cast<uint32_t*>(reinterpret_cast<const uint32_t*>(plan + L.status_off));
   p.attn_sink = opts != nullptr ? opts->attn_sink : nullptr;
   p.topk_length = opts != nullptr ? opts->topk_length : nullptr;
+  p.partials_bf16 = opts != nullptr && opts->partials_bf16 != 0 ? 1 : 0;
   p.b = dims->b;
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;
@@ -238,6 +242,7 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.attn_sink = opts != nullptr ? opts->attn_sink : nullptr;
+  p.partials_bf16 = opts != nullptr && opts->partials_bf16 != 0 ? 1 : 0;
   p.b = dims->b;
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;

@@ -197,15 +197,17 @@ struct RowCopy {
 };
 static_assert(8 * RING * RowCopy<true>::kBytes <= RAW_BYTES, "row ring");
 
-// Index of one slot, -1 for a slot past the list or past the token's topk_length (both
-// loads are issued before either is tested).
+// Index of one slot, -1 for a slot past the list or (kLen: the kernel instance for per-token
+// lengths) past the token's topk_length; both loads are issued before either is tested.  The
+// length test lives in its own instance because even an untaken test here slows the hot loop.
+template <bool kLen>
 __device__ __forceinline__ int32_t load_index(const DecodeParams& p, int s, int req, int blk,
                                               int row) {
   const int slot = blk * BT + row;
   if (slot >= p.topk) return -1;
   const size_t tok = static_cast<size_t>(req) * p.s_q + s;
   const int32_t ix = ldg_s32(p.indices + tok * p.topk + slot);
-  if (p.topk_length != nullptr && slot >= ldg_s32(p.topk_length + tok)) return -1;
+  if (kLen && slot >= ldg_s32(p.topk_length + tok)) return -1;
   return ix;
 }
 
@@ -276,7 +278,7 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
   }
 }
 
-template <bool kScores>
+template <bool kScores, bool kLen>
 __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int s, int t) {
   using RC = RowCopy<kScores>;
   const int w = t >> 5, lane = t & 31;  // warp w of the 8 dequant warps
@@ -288,7 +290,7 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
   uint32_t bad = 0;
   // Lane r < 8 holds the index of row w + 8 r of a block.
   auto idx_of = [&](const Cursor& k) -> int32_t {
-    return (lane < 8 && !k.done(pl)) ? load_index(p, s, k.req, k.blk, w + 8 * lane) : -1;
+    return (lane < 8 && !k.done(pl)) ? load_index<kLen>(p, s, k.req, k.blk, w + 8 * lane) : -1;
   };
   auto valid_bits = [&](int32_t ix) -> uint32_t {
     return __ballot_sync(0xffffffffu, lane < 8 && ix >= 0 && ix < p.num_rows) & 0xFFu;
@@ -568,18 +570,21 @@ out:
 
 // ---------------------------------------------------------------------------------------
 // O-CTA epilogue: writes O row `head` (a lane of this warp's tensor-memory quarter) for columns
-// [32 c0, 32 c1), scaled by invl: bf16 into out (unsplit request) or fp32 into the split's
-// partial.  The tensor-memory loads of the next 32 columns are in flight while the current 32
-// are scaled, converted and stored (32-byte stores when the buffers are aligned for them).
+// [32 c0, 32 c1), scaled by invl: bf16 into out (unsplit request) or into the split's partial
+// (fp32, or bf16 with partials_bf16).  The tensor-memory loads of the next 32 columns are in
+// flight while the current 32 are scaled, converted and stored (32-byte stores when the
+// buffers are aligned for them).
 __device__ void drain_o(const DecodeParams& p, uint32_t to, int head, bool no_split, int split,
                         int tok, int s, float invl, int c0, int c1) {
   const bool live = head < p.h_q;
+  const bool bf16_row = no_split || p.partials_bf16;
+  const size_t prow = (static_cast<size_t>(split) * p.s_q + s) * p.h_q + (live ? head : 0);
   uint8_t* dst_row =
       no_split ? reinterpret_cast<uint8_t*>(p.out + (static_cast<size_t>(tok) * p.h_q + (live ? head : 0)) * kDV)
-               : reinterpret_cast<uint8_t*>(p.o_accum + ((static_cast<size_t>(split) * p.s_q + s) * p.h_q + (live ? head : 0)) * kDV);
+               : reinterpret_cast<uint8_t*>(p.o_accum) + prow * kDV * (bf16_row ? 2 : 4);
   auto store_chunk = [&](const uint32_t (&o)[32], int k) {  // columns [32 k, 32 k + 32)
     if (!live) return;
-    if (no_split) {
+    if (bf16_row) {
       uint32_t v[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -627,21 +632,21 @@ __device__ void drain_o(const DecodeParams& p, uint32_t to, int head, bool no_sp
 // O-CTA epilogue of the partition's last range: the rows go through the (now unused) value-tile
 // region in the 128-byte-swizzled box layout of the output's tensor map and leave by tiled TMA
 // stores, so the store traffic is whole lines instead of one 32-byte piece per row and lane.
-// bf16 output: one pass of 8 boxes (64 columns x h_q rows); fp32 split partial: two passes of 8
-// boxes (32 columns each).  Thread `head` converts its own row and arrives on the box's barrier
+// bf16 rows (the output, or bf16 split partials): one pass of 8 boxes (64 columns x h_q rows);
+// fp32 split partial: two passes of 8 boxes (32 columns each).  Thread `head` converts its own row and arrives on the box's barrier
 // once its part of a box is written; the store issuer (role_store_issuer) sends each box as
 // soon as all rows are in, so the stores overlap the conversion.  False if a wait ran out.
 constexpr uint32_t OBOX = 16384;  // 128 rows x 128 bytes
 __device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, int head,
-                            bool no_split, float invl) {
+                            bool bf16_rows, float invl) {
   const uint32_t stage = c.sbase + OFF_TILE;
   const bool live = head < p.h_q;
   const uint32_t row = stage + static_cast<uint32_t>(head) * 128;
   const uint32_t sw = static_cast<uint32_t>(head & 7);
-  const int passes = no_split ? 1 : 2;
+  const int passes = bf16_rows ? 1 : 2;
   auto stage_chunk = [&](const uint32_t (&o)[32], int k) {  // columns [32 k, 32 k + 32)
     if (live) {
-      if (no_split) {  // 4 units of 8 bf16; box k / 2, units (k % 2) * 4 + e
+      if (bf16_rows) {  // 4 units of 8 bf16; box k / 2, units (k % 2) * 4 + e
         const uint32_t base = row + (k >> 1) * OBOX;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -664,14 +669,14 @@ __device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, in
       }
     }
     // the box is complete for this row: bf16 after its second chunk, fp32 after each chunk
-    if (!no_split || (k & 1) == 1) {
+    if (!bf16_rows || (k & 1) == 1) {
       fence_proxy_async_smem();
-      mbar_arrive(c.bar(B_OSTAGE + (no_split ? (k >> 1) : (k & 7))));
+      mbar_arrive(c.bar(B_OSTAGE + (bf16_rows ? (k >> 1) : (k & 7))));
     }
   };
   for (int pass = 0; pass < passes; ++pass) {
     if (pass > 0 && !c.wait_warp(B_OFREE, 0)) return false;
-    const int c0 = no_split ? 0 : pass * 8, c1 = no_split ? 16 : c0 + 8;
+    const int c0 = bf16_rows ? 0 : pass * 8, c1 = bf16_rows ? 16 : c0 + 8;
     uint32_t oa[32], ob[32];
     tmem_ld16(to + c0 * 32, oa);
     tmem_ld16(to + c0 * 32 + 16, oa + 16);
@@ -702,9 +707,11 @@ __device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Pla
   const int split = req == pl.begin_req ? pl.begin_split : first_slot;
   const int row0 = no_split ? (req * p.s_q + s) * p.h_q : (split * p.s_q + s) * p.h_q;
   const uint32_t stage = c.sbase + OFF_TILE;
+  const bool bf16_rows = no_split || p.partials_bf16;
   const void* map = no_split ? static_cast<const void*>(&p.out_map)
-                             : static_cast<const void*>(&p.acc_map);
-  const int passes = no_split ? 1 : 2;
+                    : bf16_rows ? static_cast<const void*>(&p.acc16_map)
+                                : static_cast<const void*>(&p.acc_map);
+  const int passes = bf16_rows ? 1 : 2;
   bool ok = true;
   for (int pass = 0; pass < passes && ok; ++pass) {
     for (int box = 0; box < 8; ++box) {
@@ -712,7 +719,7 @@ __device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Pla
         ok = false;
         break;
       }
-      tma_store_2d(map, no_split ? box * 64 : (pass * 8 + box) * 32, row0, stage + box * OBOX);
+      tma_store_2d(map, bf16_rows ? box * 64 : (pass * 8 + box) * 32, row0, stage + box * OBOX);
       bulk_commit_group();
     }
     if (ok && pass + 1 < passes) {
@@ -766,7 +773,7 @@ __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const 
     const int split = req == pl.begin_req ? pl.begin_split : first_slot;
     const int tok = req * p.s_q + s;
     if (req == pl.end_req) {  // the value tiles are free now: stage O there for TMA stores
-      if (!drain_o_tma(p, c, to, i, no_split, invl)) return;
+      if (!drain_o_tma(p, c, to, i, no_split || p.partials_bf16, invl)) return;
     } else {  // the dequant warps are already filling the tiles for the next range
       drain_o(p, to, i, no_split, split, tok, s, invl, 0, 16);
     }
@@ -788,6 +795,8 @@ __device__ void role_relay(const Ctx& c, const Plan& pl) {
     }
 }
 
+// kLen: per-token top-k lengths are given (p.topk_length is read); otherwise it is not.
+template <bool kLen>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -863,8 +872,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (scores) role_softmax(p, c, pl, s, tbase, threadIdx.x);
       else role_values_epilogue(p, c, pl, s, tbase, threadIdx.x);
     } else if (dq >= 0) {
-      if (scores) role_dequant<true>(p, c, pl, s, dq * 32 + lane);
-      else role_dequant<false>(p, c, pl, s, dq * 32 + lane);
+      if (scores) role_dequant<true, kLen>(p, c, pl, s, dq * 32 + lane);
+      else role_dequant<false, kLen>(p, c, pl, s, dq * 32 + lane);
     } else if (warp == 12) {
       if (lane == 0) {
         if (scores) role_mma_scores(c, pl, tbase);
@@ -889,7 +898,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kernel)(DecodeParams) = p.topk_length != nullptr ? decode_kernel<true> : decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: the kernel's set-up may overlap the preceding kernel;
@@ -904,7 +914,7 @@ cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, p);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace smla

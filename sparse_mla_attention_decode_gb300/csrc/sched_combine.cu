@@ -282,14 +282,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  const float* o = p.o_accum + ((static_cast<size_t>(first) * p.s_q + s) * p.h_q + h) * kDV;
+  const size_t row0 = (static_cast<size_t>(first) * p.s_q + s) * p.h_q + h;
   for (int j = 0; j < n; ++j) {
     const float w = exp2f(lse2[j * row_stride] - mx);
     wsum += w;
-    const float* oj = o + j * row_stride * kDV;
+    const size_t row = row0 + j * row_stride;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(oj + c * 128 + lane * 4);
+      float4 v;
+      if (p.partials_bf16) {  // 4 bf16 per lane: the high half of an fp32 is the bf16 value
+        const uint2 u = *reinterpret_cast<const uint2*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.o_accum) + row * kDV + c * 128 + lane * 4);
+        v = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+      } else {
+        v = *reinterpret_cast<const float4*>(p.o_accum + row * kDV + c * 128 + lane * 4);
+      }
       acc[c].x += w * v.x; acc[c].y += w * v.y; acc[c].z += w * v.z; acc[c].w += w * v.w;
     }
   }

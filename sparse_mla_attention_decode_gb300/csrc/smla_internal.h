@@ -53,6 +53,8 @@ struct DecodeParams {
   CUtensorMap out_map;
   // o_accum as rows ((split * s_q + s) * h_q + head) x 512 fp32, box 32 columns x h_q rows
   CUtensorMap acc_map;
+  // the same rows as bf16 (partials_bf16), box 64 columns x h_q rows
+  CUtensorMap acc16_map;
   const __nv_bfloat16* q;   // [b][s_q][h_q][576]
   const uint8_t* kv;        // [num_rows][656]
   const int32_t* indices;   // [b][s_q][topk]
@@ -69,6 +71,7 @@ struct DecodeParams {
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
   int store32;              // out and the workspace are 32-byte aligned (256-bit stores)
+  int partials_bf16;        // split partials of O stored as bf16 rows (else fp32)
 };
 
 struct CombineParams {
@@ -78,6 +81,7 @@ struct CombineParams {
   __nv_bfloat16* out;
   float* lse;
   const float* attn_sink;  // [h_q] or null
+  int partials_bf16;       // o_accum holds bf16 rows (else fp32)
   int b, s_q, h_q;
 };
 

@@ -17,12 +17,12 @@ LSE_ABS = 1e-3
 
 
 def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True,
-             attn_sink=None, topk_length=None):
+             attn_sink=None, topk_length=None, partials_bf16: bool = False):
     dev = wl.q.device
     op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
                               wl.kv.shape[0], device=dev, num_sms=num_sms)
     out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale, attn_sink=attn_sink,
-                      topk_length=topk_length)
+                      topk_length=topk_length, partials_bf16=partials_bf16)
     torch.cuda.synchronize(dev)
     if check_status:
         word = op.device_status()

@@ -133,3 +133,79 @@ def test_full_size_workload_with_variants(dev):
     ro, rl = gu.oracle_tokens(wl, tokens, attn_sink=sink, topk_length=lens)
     go, gl = gu.gpu_tokens(out, lse, wl, tokens)
     print(gu.compare(go, gl, ro, rl, "c2 with sink and lengths"))
+
+
+# ----------------------------------------------------------------------------- bf16 partials
+
+BF16_CASES = [
+    ("bf16p_many_splits_h128", dict(b=1, h_q=128, topk=2048, ctx=8192), 152, False),
+    ("bf16p_split_h64_sq2", dict(b=3, s_q=2, h_q=64, topk=640, ctx=4096, masked_per_row=30), 60,
+     False),
+    ("bf16p_split_sink_h128", dict(b=4, h_q=128, topk=512, ctx=4096, ue8m0=True), 120, True),
+]
+
+
+@pytest.mark.parametrize("name,kw,num_sms,use_sink", BF16_CASES, ids=[c[0] for c in BF16_CASES])
+def test_bf16_partials_parity(dev, name, kw, num_sms, use_sink):
+    seed = 900 + sum(map(ord, name))
+    wl = workloads.small(device=dev, seed=seed, **kw)
+    sink = workloads.attn_sink(wl.spec.h_q, seed, device=dev) if use_sink else None
+    out, lse, op = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, partials_bf16=True)
+    _, pre = op.plan()
+    assert int((pre[1:] - pre[:-1]).max()) > 1, "the case must have split requests"
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    ro, rl = oracle.sparse_mla_decode_full(
+        q, kv, idx, wl.sm_scale, attn_sink=None if sink is None else sink.double().cpu().numpy())
+    h = wl.spec.h_q
+    go = out.double().cpu().numpy().reshape(-1, h, 512)
+    gl = lse.double().cpu().numpy().transpose(0, 2, 1).reshape(-1, h)
+    print(name, gu.compare(go, gl, ro.reshape(-1, h, 512), rl.transpose(0, 2, 1).reshape(-1, h),
+                           name))
+    # against the fp32-partial path: the same lse, outputs a few bf16 steps apart at most
+    out32, lse32, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink)
+    assert torch.allclose(lse, lse32, rtol=0, atol=1e-5)
+    d = (out.float() - out32.float()).abs()
+    assert d.max().item() <= 4 * 2.0 ** -8 * max(1.0, out32.float().abs().max().item())
+    assert d.max().item() > 0, "the bf16-partial path gave bit-identical results"
+
+
+def test_combine_kernel_bf16_partials(dev):
+    import sparse_mla_attention_decode_gb300 as smla
+    from oracle import combine as ocomb
+    b, s_q, h = 2, 3, 128
+    op = smla.SparseMLADecode(b, s_q, h, 2048, 64, device=dev, num_sms=60)
+    st = torch.cuda.current_stream().cuda_stream
+    smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+    torch.cuda.synchronize()
+    _, pre = op.plan()
+    pre = pre.tolist()
+    parts = max(op.num_sms // s_q // 2, 1)
+    max_splits = b + parts
+    g = torch.Generator(device="cpu").manual_seed(15)
+    o_acc = torch.randn(max_splits, s_q, h, 512, generator=g).to(torch.bfloat16)
+    l_acc = torch.randn(max_splits, s_q, h, generator=g) * 3
+    l_acc[pre[0], 1, :9] = -math.inf
+    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
+    ws = op.workspace
+    ws[: o_acc.numel() * 2].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
+    ws[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
+    out = torch.full((b, s_q, h, 512), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((b, h, s_q), 7.0, dtype=torch.float32, device=dev)
+    opts = smla.smla_decode_opts(None, None, 1)
+    smla.sparse_mla_combine_ex(op.dims, op.num_sms, opts, op.sched.data_ptr(), ws.data_ptr(),
+                               op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+    torch.cuda.synchronize()
+    out, lse = out.double().cpu().numpy(), lse.double().cpu().numpy()
+    checked = 0
+    for r in range(b):
+        n = pre[r + 1] - pre[r]
+        if n <= 1:
+            continue
+        for s in range(s_q):
+            for hh in range(h):
+                ro, rl = ocomb.combine(l_acc[pre[r]:pre[r + 1], s, hh].double().numpy(),
+                                       o_acc[pre[r]:pre[r + 1], s, hh].double().numpy())
+                assert np.max(np.abs(out[r, s, hh] - ro)) <= 1e-2 * max(1, np.abs(ro).max())
+                assert abs(lse[r, hh, s] - rl) <= 1e-4
+                checked += 1
+    assert checked >= 2 * 128
