@@ -163,7 +163,7 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
  *                still pass through the pipeline).
  *   partials_bf16  nonzero: the split partials of O go through the workspace as bf16
  *                instead of fp32, halving their write and read traffic ("FlashMLA 与 DSA",
- *                section 4.2 reports this trade for a split kernel: partials are already
+ *                section 5.6 reports this trade for a split kernel: partials are already
  *                normalised by their own exp-sum, so they are bounded by the largest value
  *                element).  Results stay within the library's tolerance but differ in the
  *                last bits from the fp32 path; the workspace size is unchanged.
