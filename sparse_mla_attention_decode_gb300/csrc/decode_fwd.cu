@@ -74,10 +74,11 @@ enum Bar {
   B_O_EMPTY = B_O_FULL + 1,         // 128 epilogue threads
   B_DRAIN = B_O_EMPTY + 1,          // MMA drain on the way out
   B_STAGED = B_DRAIN + 1,           // [NMSG] 128 softmax threads wrote a message slot (S-CTA)
-  B_QLOAD = B_STAGED + NMSG,        // 1 expect-tx arrival + the bytes of the first token's Q rows
-  B_QREAD = B_QLOAD + 1,            // 128 softmax threads: Q read out of the key-tile region
+  B_QLOAD = B_STAGED + NMSG,        // [9] 1 expect-tx arrival + the bytes of one Q chunk
+  B_QREAD = B_QLOAD + 9,            // 128 softmax threads: Q read out of the key-tile region
   B_OSTAGE = B_QREAD + 1,           // [8] 128 epilogue threads staged one output box (O-CTA)
   B_OFREE = B_OSTAGE + 8,           // the stores have read the staging tiles (O-CTA)
+  B_LAST = B_OFREE + 1,             // one-shot commit after the partition's final PV (O-CTA)
   NUM_BARS
 };
 constexpr int OFF_BARS = OFF_MISC;
@@ -406,51 +407,61 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
       mma_commit(c.bar(B_VT_EMPTY + st));
       mma_commit(c.bar(B_PV_DONE + ms));
       if (blk == b1 - 1) mma_commit(c.bar(B_O_FULL));
+      if (blk == b1 - 1 && req == pl.end_req) mma_commit(c.bar(B_LAST));
     }
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// S-CTA: the Q of one query token (request number `item` of the partition) comes in by nine
-// tiled tensor copies (one per 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle) into the
-// key-tile region, and thread i = head i converts its row to fp16 and writes it to tensor
-// memory.  The region is free then: every QK of the previous request has completed and the
-// dequant warps hold the request's first tile back until B_QREAD.  The swizzle puts unit u of
-// row r at position u ^ (r % 8), so eight consecutive heads read eight distinct bank groups.
-// (Register loads of 147 KB would run at the SM's scattered-load rate.)  False if a wait ran
-// out.
+// Q of one query token (request number `item` of the partition): nine tiled tensor copies (one
+// per 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle), each with its own barrier, into
+// the key-tile region; thread i = head i converts its row to fp16 into tensor memory chunk by
+// chunk as the copies land.  The region is free then: every QK of the previous request has
+// completed and the dequant warps hold the request's first tile back until B_QREAD.  The
+// swizzle puts unit u of row r at position u ^ (r % 8), so eight consecutive heads read eight
+// distinct bank groups.  The fp16 range is checked on the bf16 magnitudes (a packed 16-bit
+// max), not per converted value: the conversion is issue-bound on the SM sub-partitions.
+// False if a wait ran out.
 static_assert(9 * 128 * 128 <= OFF_MSG, "Q fits in the key-tile region");
 __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
                              uint32_t& bad, uint32_t item) {
   const uint32_t qs = c.sbase + OFF_TILE;
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
   if (i == 0) {
-    mbar_arrive_expect_tx(c.bar(B_QLOAD), 9 * chunk_bytes);
-    for (int ch = 0; ch < 9; ++ch)
-      tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD));
-  }
-  if (!c.wait_warp(B_QLOAD, item & 1)) return false;
-  const bool live = i < p.h_q;
-  const uint32_t row = qs + (live ? i : 0) * 128;
-  const uint32_t sw = static_cast<uint32_t>(i & 7);
-#pragma unroll 1
-  for (int cc = 0; cc < 18; ++cc) {  // 18 x 32 dims = 18 x 16 columns
-    uint32_t w[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + k);
-      uint32_t in[4];
-      ld_shared_v4(row + (cc >> 1) * chunk_bytes + ((u ^ sw) << 4), in[0], in[1], in[2], in[3]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t r = pack_f16x2(__uint_as_float(in[e] << 16),
-                                      __uint_as_float(in[e] & 0xFFFF0000u));
-        bad |= ((r & 0x7C00u) == 0x7C00u) | ((r & 0x7C000000u) == 0x7C000000u);
-        w[4 * k + e] = live ? r : 0u;
-      }
+    for (int ch = 0; ch < 9; ++ch) {
+      mbar_arrive_expect_tx(c.bar(B_QLOAD + ch), chunk_bytes);
+      tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD + ch));
     }
-    tmem_st16(tq + cc * 16, w);
   }
+  const bool live = i < p.h_q;
+  const uint32_t row = qs + static_cast<uint32_t>(i) * 128;
+  const uint32_t sw = static_cast<uint32_t>(i & 7);
+  uint32_t mag[4] = {0u, 0u, 0u, 0u};  // largest bf16 magnitude seen, per 16-bit half (4 chains)
+#pragma unroll 1
+  for (int ch = 0; ch < 9; ++ch) {
+    if (!c.wait_warp(B_QLOAD + ch, item & 1)) return false;
+    uint32_t w[32];
+    if (live) {
+      uint32_t in[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        ld_shared_v4(row + ch * chunk_bytes + ((static_cast<uint32_t>(u) ^ sw) << 4), in[4 * u],
+                     in[4 * u + 1], in[4 * u + 2], in[4 * u + 3]);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        mag[e & 3] = vmax_u16x2(mag[e & 3], in[e] & 0x7FFF7FFFu);
+        w[e] = pack_f16x2(__uint_as_float(in[e] << 16), __uint_as_float(in[e] & 0xFFFF0000u));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) w[e] = 0u;
+    }
+    tmem_st16(tq + ch * 32, w);
+    tmem_st16(tq + ch * 32 + 16, w + 16);
+  }
+  // bf16 magnitude 0x4780 (2^16) and above rounds to inf in fp16 (0x477F = 65280 is finite)
+  const uint32_t m = vmax_u16x2(vmax_u16x2(mag[0], mag[1]), vmax_u16x2(mag[2], mag[3]));
+  bad |= ((m >> 16) >= 0x4780u) | ((m & 0xFFFFu) >= 0x4780u);
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(c.bar(B_Q_FULL));
@@ -632,13 +643,14 @@ __device__ void drain_o(const DecodeParams& p, uint32_t to, int head, bool no_sp
 // O-CTA epilogue of the partition's last range: the rows go through the (now unused) value-tile
 // region in the 128-byte-swizzled box layout of the output's tensor map and leave by tiled TMA
 // stores, so the store traffic is whole lines instead of one 32-byte piece per row and lane.
-// bf16 rows (the output, or bf16 split partials): one pass of 8 boxes (64 columns x h_q rows);
-// fp32 split partial: two passes of 8 boxes (32 columns each).  Thread `head` converts its own row and arrives on the box's barrier
+// bf16 rows (the output, or bf16 split partials): one pass of 8 boxes (64 columns x h_q rows),
+// whose 32-column chunks [k0, k1) this thread converts (two warpgroups share the pass); fp32
+// split partial: two passes of 8 boxes (32 columns each), all chunks.  Thread `head` converts its own row and arrives on the box's barrier
 // once its part of a box is written; the store issuer (role_store_issuer) sends each box as
 // soon as all rows are in, so the stores overlap the conversion.  False if a wait ran out.
 constexpr uint32_t OBOX = 16384;  // 128 rows x 128 bytes
 __device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, int head,
-                            bool bf16_rows, float invl) {
+                            bool bf16_rows, float invl, int k0 = 0, int k1 = 16) {
   const uint32_t stage = c.sbase + OFF_TILE;
   const bool live = head < p.h_q;
   const uint32_t row = stage + static_cast<uint32_t>(head) * 128;
@@ -676,7 +688,7 @@ __device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, in
   };
   for (int pass = 0; pass < passes; ++pass) {
     if (pass > 0 && !c.wait_warp(B_OFREE, 0)) return false;
-    const int c0 = bf16_rows ? 0 : pass * 8, c1 = bf16_rows ? 16 : c0 + 8;
+    const int c0 = bf16_rows ? k0 : pass * 8, c1 = bf16_rows ? k1 : c0 + 8;
     uint32_t oa[32], ob[32];
     tmem_ld16(to + c0 * 32, oa);
     tmem_ld16(to + c0 * 32 + 16, oa + 16);
@@ -773,13 +785,33 @@ __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const 
     const int split = req == pl.begin_req ? pl.begin_split : first_slot;
     const int tok = req * p.s_q + s;
     if (req == pl.end_req) {  // the value tiles are free now: stage O there for TMA stores
-      if (!drain_o_tma(p, c, to, i, no_split || p.partials_bf16, invl)) return;
+      // bf16 rows: this warpgroup takes columns 0-255, warps 8-11 take 256-511
+      const bool bf16_rows = no_split || p.partials_bf16;
+      if (!drain_o_tma(p, c, to, i, bf16_rows, invl, 0, bf16_rows ? 8 : 16)) return;
     } else {  // the dequant warps are already filling the tiles for the next range
       drain_o(p, to, i, no_split, split, tok, s, invl, 0, 16);
     }
     tc_fence_before();
     mbar_arrive(c.bar(B_O_EMPTY));
   }
+}
+
+// O-CTA warps 8-11 once their own roles are done: when the partition's last range leaves as
+// bf16 rows, they convert and stage columns 256-511 of it (row = their tensor-memory lane),
+// beside the epilogue warpgroup's columns 0-255.  The row's 1 / L is still in the message slot
+// of the partition's last block (no message follows it).
+__device__ void drain_o_second_half(const DecodeParams& p, const Ctx& c, const Plan& pl,
+                                    uint32_t tbase, int row) {
+  const int req = pl.end_req;
+  if (!(p.nsplits[req + 1] - p.nsplits[req] == 1 || p.partials_bf16)) return;
+  uint32_t nblk = 0;
+  for (int r = pl.begin_req; r <= pl.end_req; ++r) nblk += pl.last_block(r) - pl.first_block(r);
+  const uint32_t msg = c.sbase + OFF_MSG + ((nblk - 1) % NMSG) * MSG_STRIDE;
+  if (!c.wait_warp(B_LAST, 0)) return;
+  tc_fence_after();
+  const float invl = ld_shared_f32(msg + MSG_INVL + 4 * row);
+  const uint32_t to = tbase + (static_cast<uint32_t>((row >> 5) * 32) << 16);
+  drain_o_tma(p, c, to, row, true, invl, 8, 16);
 }
 
 // O-CTA relay lane: once a block's PV has finished reading its message slot, hand the slot
@@ -834,10 +866,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(c.bar(B_S_EMPTY + b), 128);
     }
     mbar_init(c.bar(B_Q_FULL), 128);
-    mbar_init(c.bar(B_QLOAD), 1);
+    for (int b = 0; b < 9; ++b) mbar_init(c.bar(B_QLOAD + b), 1);
     mbar_init(c.bar(B_QREAD), 128);
     for (int b = 0; b < 8; ++b) mbar_init(c.bar(B_OSTAGE + b), 128);
     mbar_init(c.bar(B_OFREE), 1);
+    mbar_init(c.bar(B_LAST), 1);
+
     mbar_init(c.bar(B_O_FULL), 1);
     mbar_init(c.bar(B_O_EMPTY), 128);
     mbar_init(c.bar(B_DRAIN), 1);
@@ -886,6 +920,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     } else if (warp == 4) {
       if (!scores && lane == 0) role_store_issuer(p, c, pl, s);
     }
+    __syncwarp();
+    if (!scores && warp >= 8 && warp < 12) drain_o_second_half(p, c, pl, tbase, (warp & 3) * 32 + lane);
 
   }
   tc_fence_before();
