@@ -136,7 +136,8 @@ smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void
  * step 16; "FlashMLA 与 DSA", section 3.2): per (token, head) with n > 1 splits,
  * M = max_j lse2_j, w_j = 2^(lse2_j - M), out = sum_j w_j o_j / sum_j w_j (bf16),
  * lse = (M + log2 sum_j w_j) ln 2; all splits empty gives out = 0, lse = +inf.  Rows of
- * unsplit requests are left untouched.
+ * unsplit requests are left untouched; when no request is split (see
+ * sparse_mla_plan_has_splits) nothing is launched.
  *   sched_meta, workspace   as passed to sparse_mla_decode_fwd (read only)
  *   out, lse                as for sparse_mla_decode_fwd (written for split rows)
  * Asynchronous on stream; must follow sparse_mla_decode_fwd on the same stream.
@@ -228,6 +229,16 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
 smla_status sparse_mla_decode_static(const smla_dims* dims, int num_sms, const void* q,
                                      const void* kv_cache, const int32_t* indices,
                                      float sm_scale, void* out, float* lse, void* stream);
+
+/*
+ * sparse_mla_plan_has_splits -- whether the plan of these sizes splits any request across
+ * partitions (*has_splits = 1), that is whether sparse_mla_combine has work.  Host-only and
+ * exact: every request has the same ceil(topk / 64) blocks, so the greedy plan of
+ * sparse_mla_sched_meta splits a request in its first partition or nowhere.  When it returns
+ * 0, sparse_mla_combine launches nothing.  Errors: SMLA_ERR_INVALID_ARG,
+ * SMLA_ERR_UNSUPPORTED, SMLA_ERR_CUDA (device query for num_sms <= 0).
+ */
+smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* sparse_mla_status_string(smla_status status);

@@ -21,6 +21,7 @@ __all__ = [
     "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
     "sparse_mla_version", "sparse_mla_decode_static", "STATIC_SCRATCH_BYTES",
     "smla_decode_opts", "sparse_mla_decode_fwd_ex", "sparse_mla_combine_ex",
+    "sparse_mla_plan_has_splits",
     "SparseMLADecode", "dims_for",
 ]
 
@@ -36,7 +37,7 @@ SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
             "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
-            "sparse_mla_combine_ex"]
+            "sparse_mla_combine_ex", "sparse_mla_plan_has_splits"]
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -91,6 +92,7 @@ def lib():
                                                    sz, vp, vp, vp]
             L.sparse_mla_combine_ex.argtypes = [P(smla_dims), ctypes.c_int, P(smla_decode_opts),
                                                 vp, vp, sz, vp, vp, vp]
+            L.sparse_mla_plan_has_splits.argtypes = [P(smla_dims), ctypes.c_int, P(ctypes.c_int)]
             L.sparse_mla_status_string.argtypes = [ctypes.c_int]
             L.sparse_mla_status_string.restype = ctypes.c_char_p
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
@@ -183,6 +185,14 @@ def sparse_mla_decode_static(dims: smla_dims, num_sms: int, q: int, kv_cache: in
         raise SparseMLAError(rc, f"sparse_mla_decode_static: the problem needs {need} bytes of "
                                  f"scratch, the fixed scratch holds {STATIC_SCRATCH_BYTES}")
     _check(rc, "sparse_mla_decode_static")
+
+
+def sparse_mla_plan_has_splits(dims: smla_dims, num_sms: int) -> bool:
+    """Whether the plan splits any request (host-only; then sparse_mla_combine has work)."""
+    v = ctypes.c_int()
+    _check(lib().sparse_mla_plan_has_splits(ctypes.byref(dims), int(num_sms), ctypes.byref(v)),
+           "sparse_mla_plan_has_splits")
+    return bool(v.value)
 
 
 def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int,

@@ -69,6 +69,22 @@ smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
   return SMLA_OK;
 }
 
+// Whether the greedy plan of these sizes splits any request, in closed form.  Every request has
+// the same nb = ceil(topk / 64) blocks and costs c = nb + 5, every partition has the same
+// payload P = ceil(b c / parts) + 5.  The first partition takes k = floor(P / c) whole requests
+// and then splits the next one exactly when more than the overhead of 5 is left (P mod c > 5,
+// which includes P < c) and a request is left (b > k).  A partition that closes at a request
+// boundary leaves the next one starting the same way, so either the first partition splits a
+// request or no partition does.
+bool plan_splits(int64_t b, int topk, int parts) {
+  const int64_t nb = (static_cast<int64_t>(topk) + kPage - 1) / kPage;
+  if (b <= 0 || nb <= 0) return false;
+  const int64_t c = nb + kFixedOverhead;
+  const int64_t P = (b * c + parts - 1) / parts + kFixedOverhead;
+  const int64_t k = P / c;
+  return P - k * c > kFixedOverhead && b > k;
+}
+
 smla_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return SMLA_OK;
   (void)cudaGetLastError();
@@ -234,6 +250,8 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
   const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
+  // no request is split: the decode pass wrote every row, so nothing is launched
+  if (!plan_splits(dims->b, dims->topk, parts)) return SMLA_OK;
   const PlanLayout L = plan_layout(dims->b, parts);
   CombineParams p;
   p.o_accum = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + A.o_off);
@@ -247,6 +265,16 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;
   return cuda_status(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits) {
+  smla_status st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  if (!has_splits) return SMLA_ERR_INVALID_ARG;
+  int parts = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  *has_splits = plan_splits(dims->b, dims->topk, parts) ? 1 : 0;
+  return SMLA_OK;
 }
 
 smla_status sparse_mla_read_device_status(const smla_dims* dims, int num_sms,

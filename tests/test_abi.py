@@ -138,3 +138,21 @@ def test_product_path_does_not_touch_the_oracle():
         if f.endswith((".py", ".c")):
             txt = open(os.path.join(ROOT, "oracle", f), encoding="utf-8").read()
             assert "sparse_mla_attention_decode_gb300" not in txt and "sparse_mla.h" not in txt, f
+
+
+def test_plan_has_splits_matches_oracle_planner(L):
+    """The host-side closed form agrees with the oracle's greedy planner (any request split)."""
+    from oracle import sched as osched
+    rng = __import__("random").Random(5)
+    cases = [(2, 1, 128, 132), (64, 1, 2048, 152), (32, 1, 2048, 152), (128, 2, 2048, 152),
+             (1, 4096, 2048, 152), (76, 1, 2048, 152), (77, 1, 2048, 152), (1, 1, 1, 152),
+             (300, 1, 2048, 152), (64, 1, 4096, 152), (5, 1, 64, 16), (200, 1, 64, 6)]
+    cases += [(rng.randint(1, 400), rng.choice([1, 1, 2, 3, 4]), rng.randint(1, 5000),
+               rng.randint(2, 300)) for _ in range(400)]
+    for b, s_q, topk, num_sms in cases:
+        d = smla.dims_for(b, s_q, 128, topk, 64)
+        got = smla.sparse_mla_plan_has_splits(d, num_sms)
+        parts = osched.num_sm_parts(num_sms, s_q)
+        _, prefix = osched.plan([topk] * b, parts)
+        want = any(prefix[i + 1] - prefix[i] > 1 for i in range(b))
+        assert got == want, (b, s_q, topk, num_sms)
