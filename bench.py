@@ -271,6 +271,7 @@ def main():
         smla.sparse_mla_combine(d, num_sms, op.sched.data_ptr(), op.workspace.data_ptr(),
                                 op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
 
+    launches_per_step = 3 if smla.sparse_mla_plan_has_splits(d, num_sms) else 2
     # One step = plan + decode + combine, back to back on the stream (events only around the
     # whole step, so the launches overlap as they do in use).
     def step(ev=None):
@@ -403,7 +404,8 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "q and indices host->device, out and lse device->host each step; "
                             "the KV cache stays resident"},
-            "gpu_launches": 3 * args.steps,  # in the timed steps (the decode-only pass adds 3 more per step)
+            # planner + decode (+ combine when a request is split) per timed step
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
