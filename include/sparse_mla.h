@@ -60,7 +60,10 @@ typedef enum {
 
 /* Problem sizes.  Only d_qk = 576, d_v = 512, page_block_size = 64, h_q in {64, 128} are
  * supported ("FlashMLA 与 DSA", section 3.1: the 656-byte V3.2 row; section 6.1: h_q 64/128,
- * d_v 512).  topk may be any value >= 0; b or s_q = 0 is an empty problem. */
+ * d_v 512).  topk may be any value >= 0; b or s_q = 0 is an empty problem.  extra_topk and
+ * extra_num_blocks size the optional second cache and index list (smla_decode_opts); 0 when
+ * it is not used.  The plan covers ceil(topk / 64) + ceil(extra_topk / 64) blocks per
+ * request ("FlashMLA 与 DSA", section 3.2 counts topk + extra_topk). */
 typedef struct {
   int32_t b;               /* batch (requests) */
   int32_t s_q;             /* query tokens per request */
@@ -70,6 +73,8 @@ typedef struct {
   int32_t topk;            /* index slots per query token */
   int32_t page_block_size; /* 64 tokens per cache page */
   int64_t num_blocks;      /* pages in the KV cache pool; num_blocks * 64 <= 2^31 - 1 */
+  int32_t extra_topk;      /* index slots per query token in the extra list (0: none) */
+  int64_t extra_num_blocks; /* pages in the extra KV cache pool; * 64 <= 2^31 - 1 */
 } smla_dims;
 
 /*
@@ -162,6 +167,15 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
  *                keeps every slot, a length <= 0 masks the whole row.  The plan still
  *                covers all topk slots (masked slots cost no cache reads, but their blocks
  *                still pass through the pipeline).
+ *   extra_kv_cache, extra_indices, extra_topk_length
+ *                the second cache ("FlashMLA 与 DSA", sections 3.2 and 6.1 name an extra_kv
+ *                beside the main cache): device uint8 [extra_num_blocks][64][1][656] in the
+ *                main cache's row format, 16-byte aligned; device int32
+ *                [b][s_q][extra_topk] physical ids into it (masked outside [0,
+ *                extra_num_blocks * 64)), 4-byte aligned; optional device int32 [b][s_q]
+ *                lengths for that list (as topk_length).  The attention runs over the union
+ *                of the main and the extra slots.  Required when dims->extra_topk > 0 (the
+ *                cache pointer only when extra_num_blocks > 0).
  *   partials_bf16  nonzero: the split partials of O go through the workspace as bf16
  *                instead of fp32, halving their write and read traffic ("FlashMLA 与 DSA",
  *                section 5.6 reports this trade for a split kernel: partials are already
@@ -176,6 +190,9 @@ typedef struct {
   const float* attn_sink;
   const int32_t* topk_length;
   int32_t partials_bf16;
+  const void* extra_kv_cache;
+  const int32_t* extra_indices;
+  const int32_t* extra_topk_length;
 } smla_decode_opts;
 
 /* sparse_mla_decode_fwd with decode options (opts may be NULL: then identical to it).

@@ -107,7 +107,8 @@ def decode_row(row: np.ndarray) -> np.ndarray:
 
 def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, sm_scale: float,
                       tokens=None, slot_range=None, threads: int = 0, attn_sink=None,
-                      topk_length=None):
+                      topk_length=None, extra_kv=None, extra_indices=None,
+                      extra_topk_length=None):
     """Sparse MLA decode in fp64.
 
     q_bits:  uint16 bf16 bit patterns [b, s_q, h_q, 576]
@@ -117,6 +118,9 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
     slot_range: optional (begin, end) sub-range of the top-k slots (one split's share)
     attn_sink:   optional per-head sink values [h_q] (``variants``); whole rows only
     topk_length: optional per-token valid prefix lengths [b, s_q] (``variants``)
+    extra_kv, extra_indices, extra_topk_length: optional second cache and slot list, joined
+                 after the main list (``variants.join_extra``); slot_range then indexes the
+                 joined list
 
     Returns (out fp64 [n_tok, h_q, 512], lse fp64 [n_tok, h_q], n_valid int32 [n_tok])
     where n_tok runs over ``tokens`` in order.
@@ -129,6 +133,9 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
     num_blocks, page = kv.shape[0], kv.shape[1]
     if topk_length is not None:
         indices = variants.mask_beyond_length(indices, topk_length)
+    if extra_indices is not None:
+        kv, indices = variants.join_extra(kv, indices, extra_kv, extra_indices, extra_topk_length)
+        num_blocks, page = kv.shape[0], kv.shape[1]
     indices = np.ascontiguousarray(indices, dtype=np.int32)
     assert indices.shape[:2] == (b, s_q)
     topk = indices.shape[2]
@@ -154,10 +161,13 @@ def sparse_mla_decode(q_bits: np.ndarray, kv: np.ndarray, indices: np.ndarray, s
 
 
 def sparse_mla_decode_full(q_bits, kv, indices, sm_scale, threads: int = 0, attn_sink=None,
-                           topk_length=None):
+                           topk_length=None, extra_kv=None, extra_indices=None,
+                           extra_topk_length=None):
     """Whole-problem form with the library's output layouts: out [b, s_q, h_q, 512],
     lse [b, h_q, s_q]."""
     b, s_q, h_q, _ = q_bits.shape
     out, lse, _ = sparse_mla_decode(q_bits, kv, indices, sm_scale, threads=threads,
-                                    attn_sink=attn_sink, topk_length=topk_length)
+                                    attn_sink=attn_sink, topk_length=topk_length,
+                                    extra_kv=extra_kv, extra_indices=extra_indices,
+                                    extra_topk_length=extra_topk_length)
     return out.reshape(b, s_q, h_q, D_V), lse.reshape(b, s_q, h_q).transpose(0, 2, 1).copy()

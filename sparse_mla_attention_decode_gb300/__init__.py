@@ -51,14 +51,18 @@ class SparseMLAError(RuntimeError):
 class smla_dims(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int32), ("s_q", ctypes.c_int32), ("h_q", ctypes.c_int32),
                 ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32),
-                ("page_block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64)]
+                ("page_block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
+                ("extra_topk", ctypes.c_int32), ("extra_num_blocks", ctypes.c_int64)]
 
 
 class smla_decode_opts(ctypes.Structure):
     """Optional decode inputs: device pointers (0 = variant off) to fp32 attn_sink [h_q] and
-    int32 topk_length [b, s_q]; partials_bf16 != 0 keeps split partials in bf16."""
+    int32 topk_length [b, s_q]; partials_bf16 != 0 keeps split partials in bf16; the extra
+    cache (uint8 [extra_num_blocks, 64, 1, 656]), its indices (int32 [b, s_q, extra_topk]) and
+    optional lengths (int32 [b, s_q])."""
     _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p),
-                ("partials_bf16", ctypes.c_int32)]
+                ("partials_bf16", ctypes.c_int32), ("extra_kv_cache", ctypes.c_void_p),
+                ("extra_indices", ctypes.c_void_p), ("extra_topk_length", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -204,8 +208,9 @@ def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int
     return rc, code.value
 
 
-def dims_for(b: int, s_q: int, h_q: int, topk: int, num_blocks: int) -> smla_dims:
-    return smla_dims(b, s_q, h_q, 576, 512, topk, 64, num_blocks)
+def dims_for(b: int, s_q: int, h_q: int, topk: int, num_blocks: int, extra_topk: int = 0,
+             extra_num_blocks: int = 0) -> smla_dims:
+    return smla_dims(b, s_q, h_q, 576, 512, topk, 64, num_blocks, extra_topk, extra_num_blocks)
 
 
 class SparseMLADecode:
@@ -214,24 +219,27 @@ class SparseMLADecode:
     q: bf16 [b, s_q, h_q, 576]; kv_cache: uint8 [num_blocks, 64, 1, 656]; indices: int32
     [b, s_q, topk]; returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, h_q, s_q]).
     Optional ``attn_sink`` (fp32 [h_q]) and ``topk_length`` (int32 [b, s_q]) device tensors
-    and ``partials_bf16`` select the decode variants of ``smla_decode_opts``.
+    and ``partials_bf16`` select the decode variants of ``smla_decode_opts``; a problem built
+    with ``extra_topk`` > 0 takes ``extra_kv`` (uint8 [extra_num_blocks, 64, 1, 656]),
+    ``extra_indices`` (int32 [b, s_q, extra_topk]) and optionally ``extra_topk_length``.
     """
 
     def __init__(self, b: int, s_q: int, h_q: int, topk: int, num_blocks: int, device=None,
-                 num_sms: int = 0):
+                 num_sms: int = 0, extra_topk: int = 0, extra_num_blocks: int = 0):
         import torch
         self.device = torch.device(device if device is not None else "cuda")
         if num_sms <= 0:
             num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.num_sms = int(num_sms)
-        self.dims = dims_for(b, s_q, h_q, topk, num_blocks)
+        self.dims = dims_for(b, s_q, h_q, topk, num_blocks, extra_topk, extra_num_blocks)
         sb, ab = sparse_mla_workspace_size(self.dims, self.num_sms)
         self.sched_bytes, self.accum_bytes = sb, ab
         self.sched = torch.empty(max(sb, 16), dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(max(ab, 16), dtype=torch.uint8, device=self.device)
 
     def run(self, q, kv_cache, indices, sm_scale: float, out=None, lse=None, stream=None,
-            attn_sink=None, topk_length=None, partials_bf16: bool = False):
+            attn_sink=None, topk_length=None, partials_bf16: bool = False, extra_kv=None,
+            extra_indices=None, extra_topk_length=None):
         import torch
         d = self.dims
         if out is None:
@@ -244,7 +252,14 @@ class SparseMLADecode:
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
         opts = None
-        if attn_sink is not None or topk_length is not None or partials_bf16:
+        if d.extra_topk > 0 and extra_indices is None:
+            raise ValueError("this problem has an extra list: pass extra_kv and extra_indices")
+        for name, t in (("extra_kv", extra_kv), ("extra_indices", extra_indices),
+                        ("extra_topk_length", extra_topk_length)):
+            if t is not None and not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        if (attn_sink is not None or topk_length is not None or partials_bf16
+                or extra_indices is not None):
             if attn_sink is not None and (attn_sink.dtype != torch.float32
                                           or attn_sink.numel() != d.h_q
                                           or not attn_sink.is_contiguous()):
@@ -253,9 +268,13 @@ class SparseMLADecode:
                                             or topk_length.numel() != d.b * d.s_q
                                             or not topk_length.is_contiguous()):
                 raise ValueError("topk_length must be a contiguous int32 tensor [b, s_q]")
-            opts = smla_decode_opts(attn_sink.data_ptr() if attn_sink is not None else None,
-                                    topk_length.data_ptr() if topk_length is not None else None,
-                                    1 if partials_bf16 else 0)
+            opts = smla_decode_opts(
+                attn_sink.data_ptr() if attn_sink is not None else None,
+                topk_length.data_ptr() if topk_length is not None else None,
+                1 if partials_bf16 else 0,
+                extra_kv.data_ptr() if extra_kv is not None else None,
+                extra_indices.data_ptr() if extra_indices is not None else None,
+                extra_topk_length.data_ptr() if extra_topk_length is not None else None)
         sparse_mla_sched_meta(d, self.num_sms, self.sched.data_ptr(), self.sched_bytes, st)
         sparse_mla_decode_fwd_ex(d, self.num_sms, q.data_ptr(), kv_cache.data_ptr(),
                                  indices.data_ptr(), sm_scale, opts, self.sched.data_ptr(),

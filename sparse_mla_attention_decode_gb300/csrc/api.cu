@@ -14,14 +14,25 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The plan's slot count per request: the main list rounded up to whole 64-slot blocks, then the
+// extra list (its blocks follow the main ones).
+int64_t plan_topk(const smla_dims* d) {
+  const int64_t nb_main = (static_cast<int64_t>(d->topk) + kPage - 1) / kPage;
+  return nb_main * kPage + d->extra_topk;
+}
+
 smla_status check_dims(const smla_dims* d) {
   if (!d) return SMLA_ERR_INVALID_ARG;
-  if (d->b < 0 || d->s_q < 0 || d->topk < 0 || d->num_blocks < 0) return SMLA_ERR_INVALID_ARG;
+  if (d->b < 0 || d->s_q < 0 || d->topk < 0 || d->num_blocks < 0 || d->extra_topk < 0 ||
+      d->extra_num_blocks < 0)
+    return SMLA_ERR_INVALID_ARG;
   if (d->h_q != 64 && d->h_q != 128) return SMLA_ERR_UNSUPPORTED;
   if (d->d_qk != kDQk || d->d_v != kDV || d->page_block_size != kPage) return SMLA_ERR_UNSUPPORTED;
   if (d->num_blocks * static_cast<int64_t>(kPage) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
+  if (d->extra_num_blocks * static_cast<int64_t>(kPage) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
+  if (plan_topk(d) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
   const int64_t tokens = static_cast<int64_t>(d->b) * d->s_q;
-  if (tokens > INT32_MAX / 128 || static_cast<int64_t>(d->topk) * tokens > (int64_t(1) << 40))
+  if (tokens > INT32_MAX / 128 || plan_topk(d) * tokens > (int64_t(1) << 40))
     return SMLA_ERR_UNSUPPORTED;
   if (d->s_q > 65535) return SMLA_ERR_UNSUPPORTED;  // grid.y
   return SMLA_OK;
@@ -30,7 +41,9 @@ smla_status check_dims(const smla_dims* d) {
 // Option pointers are optional; those given must be 4-byte aligned (fp32 / int32 arrays).
 smla_status check_opts(const smla_decode_opts* o) {
   if (o == nullptr) return SMLA_OK;
-  if (!aligned(o->attn_sink, 4) || !aligned(o->topk_length, 4)) return SMLA_ERR_ALIGNMENT;
+  if (!aligned(o->attn_sink, 4) || !aligned(o->topk_length, 4) || !aligned(o->extra_kv_cache, 16) ||
+      !aligned(o->extra_indices, 4) || !aligned(o->extra_topk_length, 4))
+    return SMLA_ERR_ALIGNMENT;
   return SMLA_OK;
 }
 
@@ -76,7 +89,7 @@ smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
 // which includes P < c) and a request is left (b > k).  A partition that closes at a request
 // boundary leaves the next one starting the same way, so either the first partition splits a
 // request or no partition does.
-bool plan_splits(int64_t b, int topk, int parts) {
+bool plan_splits(int64_t b, int64_t topk, int parts) {
   const int64_t nb = (static_cast<int64_t>(topk) + kPage - 1) / kPage;
   if (b <= 0 || nb <= 0) return false;
   const int64_t c = nb + kFixedOverhead;
@@ -152,7 +165,7 @@ smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sche
   if (dims->b == 0) {  // empty problem: only the status word needs clearing
     return cuda_status(cudaMemsetAsync(base + L.status_off, 0, 16, static_cast<cudaStream_t>(stream)));
   }
-  return cuda_status(launch_sched(dims->b, dims->s_q, dims->topk, parts,
+  return cuda_status(launch_sched(dims->b, dims->s_q, static_cast<int>(plan_topk(dims)), parts,
                                   reinterpret_cast<int32_t*>(base + L.meta_off),
                                   reinterpret_cast<int32_t*>(base + L.prefix_off),
                                   reinterpret_cast<uint32_t*>(base + L.status_off),
@@ -179,6 +192,10 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   if (tokens == 0) return SMLA_OK;
   if (!q || !sched_meta || !out || !lse || !workspace) return SMLA_ERR_INVALID_ARG;
   if (dims->topk > 0 && (!indices || (dims->num_blocks > 0 && !kv_cache))) return SMLA_ERR_INVALID_ARG;
+  const bool extra = dims->extra_topk > 0;
+  if (extra && (!opts || !opts->extra_indices ||
+                (dims->extra_num_blocks > 0 && !opts->extra_kv_cache)))
+    return SMLA_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return SMLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 16) ||
       !aligned(sched_meta, 16) || !aligned(indices, 4) || !aligned(lse, 4))
@@ -189,7 +206,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dims->topk == 0)
+  if (plan_topk(dims) == 0)
     return cuda_status(launch_fill_empty(static_cast<__nv_bfloat16*>(out), lse,
                                          tokens * dims->h_q, tokens * dims->h_q, s));
   const PlanLayout L = plan_layout(dims->b, parts);
@@ -221,6 +238,13 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;
   p.topk = dims->topk;
+  p.extra_kv = extra ? static_cast<const uint8_t*>(opts->extra_kv_cache) : nullptr;
+  p.extra_indices = extra ? opts->extra_indices : nullptr;
+  p.extra_topk_length = extra ? opts->extra_topk_length : nullptr;
+  p.extra_topk = dims->extra_topk;
+  p.extra_rows = static_cast<int>(dims->extra_num_blocks * kPage);
+  p.nb_main = (dims->topk + kPage - 1) / kPage;
+  p.nb_total = static_cast<int>((plan_topk(dims) + kPage - 1) / kPage);
   p.num_rows = static_cast<int>(dims->num_blocks * kPage);
   p.store32 = aligned(out, 32) && aligned(workspace, 32) ? 1 : 0;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 / 256.0);
@@ -241,7 +265,7 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   smla_status st = check_dims(dims);
   if (st != SMLA_OK) return st;
   const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
-  if (tokens == 0 || dims->topk == 0) return SMLA_OK;
+  if (tokens == 0 || plan_topk(dims) == 0) return SMLA_OK;
   if (!sched_meta || !workspace || !out || !lse) return SMLA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(workspace, 16) || !aligned(sched_meta, 16) || !aligned(lse, 4))
     return SMLA_ERR_ALIGNMENT;
@@ -251,7 +275,7 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
   // no request is split: the decode pass wrote every row, so nothing is launched
-  if (!plan_splits(dims->b, dims->topk, parts)) return SMLA_OK;
+  if (!plan_splits(dims->b, plan_topk(dims), parts)) return SMLA_OK;
   const PlanLayout L = plan_layout(dims->b, parts);
   CombineParams p;
   p.o_accum = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + A.o_off);
@@ -273,7 +297,7 @@ smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* 
   if (!has_splits) return SMLA_ERR_INVALID_ARG;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
-  *has_splits = plan_splits(dims->b, dims->topk, parts) ? 1 : 0;
+  *has_splits = plan_splits(dims->b, plan_topk(dims), parts) ? 1 : 0;
   return SMLA_OK;
 }
 

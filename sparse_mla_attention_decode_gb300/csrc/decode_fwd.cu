@@ -212,13 +212,25 @@ __device__ __forceinline__ int32_t load_index(const DecodeParams& p, int s, int 
   return ix;
 }
 
+// The same for the extra list (block `blk` of it; kernel instances with an extra cache only).
+__device__ __forceinline__ int32_t load_extra_index(const DecodeParams& p, int s, int req,
+                                                    int blk, int row) {
+  const int slot = blk * BT + row;
+  if (slot >= p.extra_topk) return -1;
+  const size_t tok = static_cast<size_t>(req) * p.s_q + s;
+  const int32_t ix = ldg_s32(p.extra_indices + tok * p.extra_topk + slot);
+  if (p.extra_topk_length != nullptr && slot >= ldg_s32(p.extra_topk_length + tok)) return -1;
+  return ix;
+}
+
 // Copies this lane's share of one row (j = lane % 8) into its ring slot; one commit group per
 // call covers the four rows of the warp step.
 template <bool kScores>
 __device__ __forceinline__ void issue_rows(const DecodeParams& p, int32_t idx, uint32_t slot,
-                                           int j) {
-  const bool ok = idx >= 0 && idx < p.num_rows;
-  const uint8_t* src = p.kv + static_cast<size_t>(ok ? idx : 0) * kRowBytes;
+                                           int j, bool extra = false) {
+  const uint8_t* base = extra ? p.extra_kv : p.kv;
+  const bool ok = idx >= 0 && idx < (extra ? p.extra_rows : p.num_rows);
+  const uint8_t* src = base + static_cast<size_t>(ok ? idx : 0) * kRowBytes;
   const uint32_t n = ok ? 16u : 0u;
 #pragma unroll
   for (int k = 0; k < 4; ++k) cp_async16(slot + (j + 8 * k) * 16, src + (j + 8 * k) * 16, n);
@@ -279,7 +291,9 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
   }
 }
 
-template <bool kScores, bool kLen>
+// kExtra: the kernel instance with an extra cache, whose blocks follow the main list's in the
+// plan (blocks nb_main and up read the extra indices and rows).
+template <bool kScores, bool kLen, bool kExtra>
 __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int s, int t) {
   using RC = RowCopy<kScores>;
   const int w = t >> 5, lane = t & 31;  // warp w of the 8 dequant warps
@@ -289,23 +303,28 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
   const int stage_bytes = kScores ? KT_STAGE : VT_STAGE;
   const uint32_t ring = c.sbase + OFF_RAW + w * RING * RC::kBytes;
   uint32_t bad = 0;
+  auto in_extra = [&](const Cursor& k) -> bool { return kExtra && k.blk >= p.nb_main; };
   // Lane r < 8 holds the index of row w + 8 r of a block.
   auto idx_of = [&](const Cursor& k) -> int32_t {
-    return (lane < 8 && !k.done(pl)) ? load_index<kLen>(p, s, k.req, k.blk, w + 8 * lane) : -1;
+    if (lane >= 8 || k.done(pl)) return -1;
+    if (in_extra(k)) return load_extra_index(p, s, k.req, k.blk - p.nb_main, w + 8 * lane);
+    return load_index<kLen>(p, s, k.req, k.blk, w + 8 * lane);
   };
-  auto valid_bits = [&](int32_t ix) -> uint32_t {
-    return __ballot_sync(0xffffffffu, lane < 8 && ix >= 0 && ix < p.num_rows) & 0xFFu;
+  auto valid_bits = [&](int32_t ix, bool extra) -> uint32_t {
+    const int rows = extra ? p.extra_rows : p.num_rows;
+    return __ballot_sync(0xffffffffu, lane < 8 && ix >= 0 && ix < rows) & 0xFFu;
   };
   Cursor cur, fetch;
   cur.start(pl);
   fetch = cur;
   // prologue: the first block's rows in flight, the second block's indices loaded
   const int32_t ix0 = idx_of(fetch);
-  uint32_t vmask = valid_bits(ix0);  // bits 8 k + r: row r of block cur + k is valid
+  uint32_t vmask = valid_bits(ix0, in_extra(fetch));  // bits 8 k + r: row r of block cur + k is valid
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = 4 * h + rsel;
-    issue_rows<kScores>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j);
+    issue_rows<kScores>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j,
+                        in_extra(fetch));
   }
   fetch.next(pl);
   int32_t ixA = idx_of(fetch);  // block cur + 1
@@ -317,8 +336,9 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     Cursor ah = cur;
     ah.next(pl);
     const bool issue_more = !ah.done(pl);  // block cur + 1 exists
+    const bool extra_next = in_extra(ah);
     const int32_t ixB = idx_of(fetch);      // block cur + 2, loaded one block early
-    vmask |= valid_bits(ixA) << 8;
+    vmask |= valid_bits(ixA, extra_next) << 8;
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
     // each token's Q passes through the key-tile region on its way to tensor memory: the
     // first tile of a request waits until it has been read out
@@ -341,7 +361,7 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
         if (kScores) ld_shared_v4(slot + kDNope + 16 + j * 16, rope.x, rope.y, rope.z, rope.w);
         __syncwarp();  // every lane has read the slot: it can take the next block's row
         const int32_t nx = __shfl_sync(0xffffffffu, ixA, r);
-        if (issue_more) issue_rows<kScores>(p, nx, slot, j);
+        if (issue_more) issue_rows<kScores>(p, nx, slot, j, extra_next);
         else cp_async_commit();  // an empty group keeps the count per step uniform
         store_rows<kScores>(tile, w + 8 * r, j, (vmask >> r) & 1u, nope, scales, rope, bad);
       }
@@ -828,7 +848,8 @@ __device__ void role_relay(const Ctx& c, const Plan& pl) {
 }
 
 // kLen: per-token top-k lengths are given (p.topk_length is read); otherwise it is not.
-template <bool kLen>
+// kExtra: an extra cache and index list follow the main ones.
+template <bool kLen, bool kExtra>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -896,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   pl.begin_block = m[2];
   pl.end_block = m[3];
   pl.begin_split = m[4];
-  pl.nb = (p.topk + BT - 1) / BT;
+  pl.nb = p.nb_total;
   const bool active = pl.begin_req < p.b;
 
   if (active) {
@@ -906,8 +927,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (scores) role_softmax(p, c, pl, s, tbase, threadIdx.x);
       else role_values_epilogue(p, c, pl, s, tbase, threadIdx.x);
     } else if (dq >= 0) {
-      if (scores) role_dequant<true, kLen>(p, c, pl, s, dq * 32 + lane);
-      else role_dequant<false, kLen>(p, c, pl, s, dq * 32 + lane);
+      if (scores) role_dequant<true, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
+      else role_dequant<false, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
     } else if (warp == 12) {
       if (lane == 0) {
         if (scores) role_mma_scores(c, pl, tbase);
@@ -934,7 +955,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream) {
-  void (*kernel)(DecodeParams) = p.topk_length != nullptr ? decode_kernel<true> : decode_kernel<false>;
+  void (*kernel)(DecodeParams) =
+      p.extra_indices != nullptr
+          ? (p.topk_length != nullptr ? decode_kernel<true, true> : decode_kernel<false, true>)
+          : (p.topk_length != nullptr ? decode_kernel<true, false> : decode_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -67,6 +67,11 @@ struct DecodeParams {
   uint32_t* status;         // device status word
   const float* attn_sink;   // [h_q] or null
   const int32_t* topk_length;  // [b][s_q] or null
+  const uint8_t* extra_kv;        // [extra_rows][656] or null
+  const int32_t* extra_indices;   // [b][s_q][extra_topk] or null
+  const int32_t* extra_topk_length;  // [b][s_q] or null
+  int extra_topk, extra_rows;
+  int nb_main, nb_total;    // blocks of the main list; of both lists (the plan's blocks)
   int b, s_q, h_q, topk;
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)

@@ -17,12 +17,17 @@ LSE_ABS = 1e-3
 
 
 def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True,
-             attn_sink=None, topk_length=None, partials_bf16: bool = False):
+             attn_sink=None, topk_length=None, partials_bf16: bool = False, extra_kv=None,
+             extra_indices=None, extra_topk_length=None):
     dev = wl.q.device
+    ek = 0 if extra_indices is None else extra_indices.shape[-1]
+    enb = 0 if extra_kv is None else extra_kv.shape[0]
     op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
-                              wl.kv.shape[0], device=dev, num_sms=num_sms)
+                              wl.kv.shape[0], device=dev, num_sms=num_sms, extra_topk=ek,
+                              extra_num_blocks=enb)
     out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale, attn_sink=attn_sink,
-                      topk_length=topk_length, partials_bf16=partials_bf16)
+                      topk_length=topk_length, partials_bf16=partials_bf16, extra_kv=extra_kv,
+                      extra_indices=extra_indices, extra_topk_length=extra_topk_length)
     torch.cuda.synchronize(dev)
     if check_status:
         word = op.device_status()
@@ -51,6 +56,42 @@ def compact_inputs(wl: workloads.Workload, tokens: np.ndarray):
     kvn = pool.cpu().numpy().reshape(-1, 64, 656)
     idn = new_idx.to(torch.int32).cpu().numpy().reshape(n, 1, -1)
     return qb, kvn, idn
+
+
+def compact_pool(kv: torch.Tensor, idx_rows: torch.Tensor):
+    """(small pool [pages, 64, 656] numpy, renumbered int32 indices numpy) holding only the
+    rows that ``idx_rows`` [n, k] selects from ``kv``; invalid slots stay invalid."""
+    nrows = kv.shape[0] * 64
+    valid = (idx_rows >= 0) & (idx_rows < nrows)
+    used = torch.unique(idx_rows[valid])
+    remap = torch.full((max(nrows, 1),), -1, dtype=torch.int64, device=idx_rows.device)
+    remap[used] = torch.arange(used.numel(), device=idx_rows.device)
+    new_idx = torch.where(valid, remap[idx_rows.clamp(0, max(nrows - 1, 0)).long()],
+                          torch.full_like(idx_rows, -1).long())
+    npages = (used.numel() + 63) // 64
+    pool = torch.zeros(max(npages, 1) * 64, 656, dtype=torch.uint8, device=idx_rows.device)
+    if used.numel():
+        pool[: used.numel()] = kv.reshape(nrows, 656)[used]
+    return pool.cpu().numpy().reshape(-1, 64, 656), new_idx.to(torch.int32).cpu().numpy()
+
+
+def oracle_tokens_extra(wl: workloads.Workload, tokens, extra_kv, extra_indices,
+                        extra_topk_length=None, attn_sink=None, topk_length=None):
+    """oracle_tokens with an extra cache and list (both pools compacted to the used rows)."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    qb, kvn, idn = compact_inputs(wl, tokens)
+    n = len(tokens)
+    t = torch.as_tensor(tokens, device=extra_indices.device)
+    ekv, eidx = compact_pool(extra_kv, extra_indices.reshape(wl.spec.b * wl.spec.s_q, -1)[t])
+    sink = None if attn_sink is None else attn_sink.double().cpu().numpy()
+    lens = None if topk_length is None else topk_length.reshape(-1).cpu().numpy()[tokens].reshape(-1, 1)
+    elens = (None if extra_topk_length is None
+             else extra_topk_length.reshape(-1).cpu().numpy()[tokens].reshape(-1, 1))
+    out, lse, _ = oracle.sparse_mla_decode(qb, kvn, idn, wl.sm_scale, attn_sink=sink,
+                                           topk_length=lens, extra_kv=ekv,
+                                           extra_indices=eidx.reshape(n, 1, -1),
+                                           extra_topk_length=elens)
+    return out, lse
 
 
 def oracle_tokens(wl: workloads.Workload, tokens, threads: int = 0, attn_sink=None,

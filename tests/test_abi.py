@@ -53,7 +53,9 @@ def test_workspace_sizes(L):
 
 @pytest.mark.parametrize("field,value,code", [("h_q", 96, 2), ("d_qk", 512, 2), ("d_v", 256, 2),
                                               ("page_block_size", 32, 2), ("b", -1, 1),
-                                              ("topk", -5, 1), ("num_blocks", 1 << 26, 2)])
+                                              ("topk", -5, 1), ("num_blocks", 1 << 26, 2),
+                                              ("extra_topk", -1, 1),
+                                              ("extra_num_blocks", 1 << 26, 2)])
 def test_bad_dims_rejected(L, field, value, code):
     d = smla.dims_for(2, 1, 128, 128, 64)
     setattr(d, field, value)
@@ -104,7 +106,9 @@ def test_decode_option_checks_before_launch(L):
         return L.sparse_mla_combine_ex(ctypes.byref(d), 152, opts, fake, fake, ab, fake, fake,
                                        None)
 
-    for bad in (smla.smla_decode_opts(fake + 2, None), smla.smla_decode_opts(None, fake + 1)):
+    for bad in (smla.smla_decode_opts(fake + 2, None), smla.smla_decode_opts(None, fake + 1),
+                smla.smla_decode_opts(None, None, 0, fake + 8, fake),
+                smla.smla_decode_opts(None, None, 0, fake, fake + 2)):
         assert fwd(ctypes.byref(bad)) == 3
         assert comb(ctypes.byref(bad)) == 3
     # other argument errors still come first or alongside: a null q with options set
@@ -156,3 +160,20 @@ def test_plan_has_splits_matches_oracle_planner(L):
         _, prefix = osched.plan([topk] * b, parts)
         want = any(prefix[i + 1] - prefix[i] > 1 for i in range(b))
         assert got == want, (b, s_q, topk, num_sms)
+
+
+def test_extra_list_needs_its_pointers(L):
+    d = smla.dims_for(2, 1, 128, 128, 64, extra_topk=64, extra_num_blocks=8)
+    sb, ab = smla.sparse_mla_workspace_size(d, 152)
+    fake = 0x10000
+    # the plain call has no extra pointers: rejected before launch
+    assert L.sparse_mla_decode_fwd(ctypes.byref(d), 152, fake, fake, fake, ctypes.c_float(0.04),
+                                   fake, fake, ab, fake, fake, None) == 1
+    no_cache = smla.smla_decode_opts(None, None, 0, None, fake)
+    assert L.sparse_mla_decode_fwd_ex(ctypes.byref(d), 152, fake, fake, fake, ctypes.c_float(0.04),
+                                      ctypes.byref(no_cache), fake, fake, ab, fake, fake, None) == 1
+    # the plan counts both lists: 2 + 1 blocks per request
+    d0 = smla.dims_for(2, 1, 128, 128, 64)
+    d3 = smla.dims_for(2, 1, 128, 192, 64)
+    assert smla.sparse_mla_plan_has_splits(d, 152) == smla.sparse_mla_plan_has_splits(d3, 152)
+    assert smla.sparse_mla_workspace_size(d, 152) == smla.sparse_mla_workspace_size(d0, 152)

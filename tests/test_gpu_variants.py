@@ -209,3 +209,77 @@ def test_combine_kernel_bf16_partials(dev):
                 assert abs(lse[r, hh, s] - rl) <= 1e-4
                 checked += 1
     assert checked >= 2 * 128
+
+
+# ----------------------------------------------------------------------------- extra_kv
+
+def _extra_inputs(wl, extra_topk, ctx, seed, masked=0, out_of_range=0):
+    """A second cache (its own pool) and index list for the tokens of ``wl``; some slots are
+    masked and slots 3.. hold ids just past the extra pool (which must be masked, not read
+    from any other pool)."""
+    wx = workloads.small(b=wl.spec.b, s_q=wl.spec.s_q, h_q=wl.spec.h_q, topk=extra_topk,
+                         ctx=ctx, masked_per_row=masked, seed=seed, device=wl.q.device)
+    eidx = wx.indices.clone()
+    if out_of_range:
+        erows = wx.kv.shape[0] * 64
+        eidx[..., 3:3 + out_of_range] = erows + torch.arange(out_of_range, device=eidx.device,
+                                                             dtype=eidx.dtype)
+    return wx.kv.contiguous(), eidx.contiguous()
+
+
+EXTRA_CASES = [
+    # (name, main workload kwargs, extra_topk, num_sms, with lengths, with sink)
+    ("extra_nosplit_h128", dict(b=3, h_q=128, topk=200, ctx=2048, masked_per_row=10), 130, 8,
+     False, False),
+    ("extra_split_h128_lens_sink", dict(b=2, h_q=128, topk=256, ctx=2048), 192, 132, True,
+     True),
+    ("extra_split_h64_sq2", dict(b=2, s_q=2, h_q=64, topk=100, ctx=1024, causal_base=700), 77,
+     48, True, False),
+    ("extra_only_topk0", dict(b=3, h_q=128, topk=0, ctx=512), 150, 24, False, True),
+    ("extra_ragged_main", dict(b=4, h_q=128, topk=65, ctx=1024, ue8m0=True), 63, 20, True,
+     False),
+]
+
+
+@pytest.mark.parametrize("name,kw,extra_topk,num_sms,use_len,use_sink", EXTRA_CASES,
+                         ids=[c[0] for c in EXTRA_CASES])
+def test_extra_kv_parity(dev, name, kw, extra_topk, num_sms, use_len, use_sink):
+    seed = 1300 + sum(map(ord, name))
+    wl = workloads.small(device=dev, seed=seed, **kw)
+    ekv, eidx = _extra_inputs(wl, extra_topk, ctx=768, seed=seed + 1, masked=7, out_of_range=3)
+    lens = elens = sink = None
+    if use_len:
+        lens = workloads.topk_lengths(wl.spec.b, wl.spec.s_q, max(wl.spec.topk, 1), seed, device=dev)
+        elens = workloads.topk_lengths(wl.spec.b, wl.spec.s_q, extra_topk, seed + 2, device=dev)
+    if use_sink:
+        sink = workloads.attn_sink(wl.spec.h_q, seed, device=dev)
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, topk_length=lens,
+                              extra_kv=ekv, extra_indices=eidx, extra_topk_length=elens)
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    ro, rl = oracle.sparse_mla_decode_full(
+        q, kv, idx, wl.sm_scale,
+        attn_sink=None if sink is None else sink.double().cpu().numpy(),
+        topk_length=None if lens is None else lens.cpu().numpy(),
+        extra_kv=ekv.cpu().numpy().reshape(-1, 64, 656), extra_indices=eidx.cpu().numpy(),
+        extra_topk_length=None if elens is None else elens.cpu().numpy())
+    h = wl.spec.h_q
+    go = out.double().cpu().numpy().reshape(-1, h, 512)
+    gl = lse.double().cpu().numpy().transpose(0, 2, 1).reshape(-1, h)
+    print(name, gu.compare(go, gl, ro.reshape(-1, h, 512), rl.transpose(0, 2, 1).reshape(-1, h),
+                           name))
+    if wl.spec.topk > 0:  # the extra list changed the result
+        plain, _, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, topk_length=lens)
+        assert np.abs(go - plain.double().cpu().numpy().reshape(go.shape)).max() > 2 * gu.O_MAX_ABS
+
+
+def test_full_size_workload_with_extra_kv(dev):
+    spec = workloads.CONFIGS["c2_b64_h128_k2048_mask5"]
+    wl = workloads.make(spec, device=dev)
+    ekv, eidx = _extra_inputs(wl, 512, ctx=4096, seed=991, masked=20, out_of_range=2)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, extra_kv=ekv, extra_indices=eidx)
+    assert torch.isfinite(out.float()).all()
+    tokens = np.array([0, 1, 17, 31, 32, 50, 62, 63])
+    ro, rl = gu.oracle_tokens_extra(wl, tokens, ekv, eidx)
+    go, gl = gu.gpu_tokens(out, lse, wl, tokens)
+    print(gu.compare(go, gl, ro, rl, "c2 with a 512-slot extra list"))

@@ -153,3 +153,64 @@ def test_topk_length_bounds():
     assert np.all(o == 0.0) and np.all(np.isposinf(l)) and np.all(nv == 0)
     # the input array is not modified
     assert np.array_equal(idx, workloads.to_numpy_inputs(wl)[2])
+
+
+# --------------------------------------------------------------------------- extra_kv
+
+def _extra(b, s_q, h, topk, extra_topk, seed):
+    wl, q, kv, idx = _tiny(b=b, s_q=s_q, h=h, topk=topk, ctx=512, masked_per_row=3, seed=seed)
+    wx = workloads.small(b=b, s_q=s_q, h_q=h, topk=extra_topk, ctx=256, masked_per_row=2,
+                         seed=seed + 50)
+    _, ekv, eidx = workloads.to_numpy_inputs(wx)
+    return wl, q, kv, idx, ekv, eidx
+
+
+def test_extra_kv_equals_one_list_in_another_layout():
+    # the union of the two lists, rebuilt with the extra pool FIRST and the extra slots first:
+    # the same set of (query, key) pairs, so the same result
+    wl, q, kv, idx, ekv, eidx = _extra(2, 2, 4, 40, 24, seed=12)
+    out, lse, nv = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv,
+                                            extra_indices=eidx)
+    erows = ekv.shape[0] * ekv.shape[1]
+    mrows = kv.shape[0] * kv.shape[1]
+    pool = np.ascontiguousarray(np.concatenate([ekv, kv], axis=0))
+    shifted = np.where((idx >= 0) & (idx < mrows), idx + erows, -1).astype(np.int32)
+    both = np.ascontiguousarray(np.concatenate([eidx, shifted], axis=2))
+    o2, l2, nv2 = oracle.sparse_mla_decode(q, pool, both, wl.sm_scale)
+    assert _rel(out, o2) < 1e-12 and np.max(np.abs(lse - l2)) < 1e-12
+    assert np.array_equal(nv, nv2) and np.all(nv == np.sum(idx >= 0, axis=2).reshape(-1)
+                                              + np.sum(eidx >= 0, axis=2).reshape(-1))
+
+
+def test_extra_kv_alone_and_empty():
+    wl, q, kv, idx, ekv, eidx = _extra(2, 1, 3, 32, 48, seed=13)
+    none = np.full_like(idx, -1)
+    o, l, _ = oracle.sparse_mla_decode(q, kv, none, wl.sm_scale, extra_kv=ekv, extra_indices=eidx)
+    o2, l2, _ = oracle.sparse_mla_decode(q, ekv, eidx, wl.sm_scale)
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
+    plain, lp, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale)
+    o3, l3, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv,
+                                         extra_indices=np.full_like(eidx, -1))
+    assert np.array_equal(o3, plain) and np.array_equal(l3, lp)
+
+
+def test_extra_kv_masks_against_its_own_pool():
+    wl, q, kv, idx, ekv, eidx = _extra(1, 1, 2, 16, 16, seed=14)
+    erows = ekv.shape[0] * ekv.shape[1]
+    base, lb, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv,
+                                           extra_indices=eidx)
+    bad = eidx.copy()
+    bad[0, 0, :4] = [erows, erows + 3, -5, 1 << 30]  # outside the extra pool: masked
+    ref = eidx.copy()
+    ref[0, 0, :4] = -1
+    o1, l1, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv, extra_indices=bad)
+    o2, l2, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv, extra_indices=ref)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # extra_topk_length masks the extra list's tail only
+    o3, l3, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv, extra_indices=eidx,
+                                         extra_topk_length=[[5]])
+    cut = np.full_like(eidx, -1)
+    cut[..., :5] = eidx[..., :5]
+    o4, l4, _ = oracle.sparse_mla_decode(q, kv, idx, wl.sm_scale, extra_kv=ekv, extra_indices=cut)
+    assert np.array_equal(o3, o4) and np.array_equal(l3, l4)
+    assert not np.array_equal(o3, base)
