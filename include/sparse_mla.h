@@ -57,6 +57,7 @@ typedef enum {
 #define SMLA_DEV_TIMEOUT 0x1u       /* a pipeline wait gave up; outputs are not valid */
 #define SMLA_DEV_Q_RANGE 0x2u       /* |q| above 65504: not representable in the fp16 MMA */
 #define SMLA_DEV_SCALE_RANGE 0x4u   /* a KV scale * 256 outside the fp16 normal range */
+#define SMLA_DEV_TOPK_TABLE 0x8u    /* top-k: a selected position lies beyond the page table */
 
 /* Problem sizes.  Only d_qk = 576, d_v = 512, page_block_size = 64, h_q in {64, 128} are
  * supported ("FlashMLA 与 DSA", section 3.1: the 656-byte V3.2 row; section 6.1: h_q 64/128,
@@ -256,6 +257,46 @@ smla_status sparse_mla_decode_static(const smla_dims* dims, int num_sms, const v
  * SMLA_ERR_UNSUPPORTED, SMLA_ERR_CUDA (device query for num_sms <= 0).
  */
 smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits);
+
+/*
+ * sparse_mla_topk_page_table -- the step before the attention: for every query token, the
+ * exact top-k of its index scores over its valid (causally visible) prefix, emitted as
+ * physical cache ids ("FlashMLA 与 DSA", section 5.5: a two-stage filtered radix top-k whose
+ * emit writes page_table[u / 64] * 64 + u % 64 directly; "sparse-attention co-design",
+ * section 5, step five: a row with fewer than k valid tokens is padded with an invalid id,
+ * never a repeated token).  The result is the `indices` input of sparse_mla_decode_fwd.
+ *   dims->n_tok      query tokens (rows of scores); token t belongs to request t / s_q
+ *   dims->s_q        query tokens per request (rows of the page table: ceil(n_tok / s_q))
+ *   dims->topk       k, output slots per token (>= 1)
+ *   dims->ld         row stride of scores in elements; ld * element size a multiple of 16
+ *   dims->max_pages  columns of the page table
+ *   dims->dtype      SMLA_SCORES_BF16 or SMLA_SCORES_FP32
+ *   scores           device [n_tok][ld] bf16 or fp32, 16-byte aligned; finite or +-inf (NaN
+ *                    is not ordered)
+ *   valid_len        device int32 [n_tok]: token t scores positions [0, valid_len[t]) (clamped
+ *                    to [0, ld])
+ *   block_table      device int32 [ceil(n_tok / s_q)][max_pages]: page ids of each request
+ *   out_indices      device int32 [n_tok][topk] (written): the selected ids in no particular
+ *                    order, then -1 for the slots past min(k, valid_len[t]); ties at the k-th
+ *                    largest value are broken arbitrarily (any k largest are a correct answer)
+ *   status           optional device uint32 word: SMLA_DEV_TOPK_TABLE is or-ed in when a
+ *                    selected position u has u / 64 >= max_pages (that slot gets -1)
+ * Asynchronous on stream.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED (dtype),
+ * SMLA_ERR_ALIGNMENT, SMLA_ERR_CUDA.
+ */
+#define SMLA_SCORES_BF16 0
+#define SMLA_SCORES_FP32 1
+typedef struct {
+  int32_t n_tok;
+  int32_t s_q;
+  int32_t topk;
+  int32_t ld;
+  int32_t max_pages;
+  int32_t dtype;
+} smla_topk_dims;
+smla_status sparse_mla_topk_page_table(const smla_topk_dims* dims, const void* scores,
+                                       const int32_t* valid_len, const int32_t* block_table,
+                                       int32_t* out_indices, uint32_t* status, void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* sparse_mla_status_string(smla_status status);

@@ -21,7 +21,8 @@ __all__ = [
     "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
     "sparse_mla_version", "sparse_mla_decode_static", "STATIC_SCRATCH_BYTES",
     "smla_decode_opts", "sparse_mla_decode_fwd_ex", "sparse_mla_combine_ex",
-    "sparse_mla_plan_has_splits",
+    "sparse_mla_plan_has_splits", "smla_topk_dims", "sparse_mla_topk_page_table",
+    "topk_page_table", "SMLA_SCORES_BF16", "SMLA_SCORES_FP32",
     "SparseMLADecode", "dims_for",
 ]
 
@@ -33,11 +34,12 @@ _lib = None
 SMLA_OK = 0
 SMLA_ERR_WORKSPACE = 4
 SMLA_ERR_TIMEOUT = 6
-SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE = 0x1, 0x2, 0x4
+SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE, SMLA_DEV_TOPK_TABLE = 0x1, 0x2, 0x4, 0x8
+SMLA_SCORES_BF16, SMLA_SCORES_FP32 = 0, 1
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
             "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
-            "sparse_mla_combine_ex", "sparse_mla_plan_has_splits"]
+            "sparse_mla_combine_ex", "sparse_mla_plan_has_splits", "sparse_mla_topk_page_table"]
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -63,6 +65,11 @@ class smla_decode_opts(ctypes.Structure):
     _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p),
                 ("partials_bf16", ctypes.c_int32), ("extra_kv_cache", ctypes.c_void_p),
                 ("extra_indices", ctypes.c_void_p), ("extra_topk_length", ctypes.c_void_p)]
+
+
+class smla_topk_dims(ctypes.Structure):
+    _fields_ = [("n_tok", ctypes.c_int32), ("s_q", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("ld", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -97,6 +104,7 @@ def lib():
             L.sparse_mla_combine_ex.argtypes = [P(smla_dims), ctypes.c_int, P(smla_decode_opts),
                                                 vp, vp, sz, vp, vp, vp]
             L.sparse_mla_plan_has_splits.argtypes = [P(smla_dims), ctypes.c_int, P(ctypes.c_int)]
+            L.sparse_mla_topk_page_table.argtypes = [P(smla_topk_dims), vp, vp, vp, vp, vp, vp]
             L.sparse_mla_status_string.argtypes = [ctypes.c_int]
             L.sparse_mla_status_string.restype = ctypes.c_char_p
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
@@ -197,6 +205,38 @@ def sparse_mla_plan_has_splits(dims: smla_dims, num_sms: int) -> bool:
     _check(lib().sparse_mla_plan_has_splits(ctypes.byref(dims), int(num_sms), ctypes.byref(v)),
            "sparse_mla_plan_has_splits")
     return bool(v.value)
+
+
+def sparse_mla_topk_page_table(dims: smla_topk_dims, scores: int, valid_len: int,
+                               block_table: int, out_indices: int, status: int = 0,
+                               stream: int = 0) -> None:
+    _check(lib().sparse_mla_topk_page_table(ctypes.byref(dims), scores, valid_len, block_table,
+                                            out_indices, status or None, stream),
+           "sparse_mla_topk_page_table")
+
+
+def topk_page_table(scores, valid_len, block_table, s_q: int, k: int, out=None, status=None,
+                    stream=None):
+    """Exact top-k of each row of ``scores`` (bf16 or fp32 [n_tok, ld] device tensor) over its
+    first valid_len[t] positions, as physical ids through ``block_table`` (int32 [b, pages];
+    row t uses request t // s_q): int32 [n_tok, k], -1 after the selected ids."""
+    import torch
+    if scores.dim() != 2 or scores.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("scores must be a 2-D bf16 or fp32 tensor")
+    if scores.stride(1) != 1:
+        raise ValueError("scores rows must be contiguous")
+    for name, t in (("valid_len", valid_len), ("block_table", block_table)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    n_tok = scores.shape[0]
+    if out is None:
+        out = torch.empty(n_tok, k, dtype=torch.int32, device=scores.device)
+    d = smla_topk_dims(n_tok, s_q, k, scores.stride(0), block_table.shape[1],
+                       SMLA_SCORES_FP32 if scores.dtype == torch.float32 else SMLA_SCORES_BF16)
+    st = (stream if stream is not None else torch.cuda.current_stream(scores.device)).cuda_stream
+    sparse_mla_topk_page_table(d, scores.data_ptr(), valid_len.data_ptr(), block_table.data_ptr(),
+                               out.data_ptr(), status.data_ptr() if status is not None else 0, st)
+    return out
 
 
 def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int,

@@ -291,6 +291,29 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   return cuda_status(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
 
+smla_status sparse_mla_topk_page_table(const smla_topk_dims* d, const void* scores,
+                                       const int32_t* valid_len, const int32_t* block_table,
+                                       int32_t* out_indices, uint32_t* status, void* stream) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->n_tok < 0 || d->s_q < 1 || d->topk < 1 || d->ld < 0 || d->max_pages < 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->dtype != SMLA_SCORES_BF16 && d->dtype != SMLA_SCORES_FP32) return SMLA_ERR_UNSUPPORTED;
+  if (d->n_tok == 0) return SMLA_OK;
+  if (!valid_len || !block_table || !out_indices || (d->ld > 0 && !scores))
+    return SMLA_ERR_INVALID_ARG;
+  const int esize = d->dtype == SMLA_SCORES_FP32 ? 4 : 2;
+  if (!aligned(scores, 16) || (static_cast<int64_t>(d->ld) * esize) % 16 != 0 ||
+      !aligned(valid_len, 4) || !aligned(block_table, 4) || !aligned(out_indices, 4) ||
+      !aligned(status, 4))
+    return SMLA_ERR_ALIGNMENT;
+  if (static_cast<int64_t>(d->n_tok) * d->topk > INT32_MAX ||
+      static_cast<int64_t>(d->max_pages) * kPage > INT32_MAX)
+    return SMLA_ERR_UNSUPPORTED;
+  return cuda_status(launch_topk(scores, d->dtype == SMLA_SCORES_FP32, valid_len, block_table,
+                                 out_indices, status, d->n_tok, d->s_q, d->topk, d->ld,
+                                 d->max_pages, static_cast<cudaStream_t>(stream)));
+}
+
 smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits) {
   smla_status st = check_dims(dims);
   if (st != SMLA_OK) return st;

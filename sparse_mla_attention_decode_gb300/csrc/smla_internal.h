@@ -100,6 +100,9 @@ cudaError_t launch_sched(int b, int s_q, int topk, int parts, int32_t* meta, int
                          uint32_t* status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
+                        const int32_t* table, int32_t* out, uint32_t* status, int n_tok, int s_q,
+                        int k, int ld, int max_pages, cudaStream_t stream);
 cudaError_t launch_fill_empty(__nv_bfloat16* out, float* lse, int64_t rows_o, int64_t n_lse,
                               cudaStream_t stream);
 

@@ -177,3 +177,17 @@ def test_extra_list_needs_its_pointers(L):
     d3 = smla.dims_for(2, 1, 128, 192, 64)
     assert smla.sparse_mla_plan_has_splits(d, 152) == smla.sparse_mla_plan_has_splits(d3, 152)
     assert smla.sparse_mla_workspace_size(d, 152) == smla.sparse_mla_workspace_size(d0, 152)
+
+
+def test_topk_argument_checks(L):
+    fake = 0x10000
+    d = smla.smla_topk_dims(4, 1, 64, 128, 2, smla.SMLA_SCORES_BF16)
+    call = lambda dd, sc=fake: L.sparse_mla_topk_page_table(ctypes.byref(dd), sc, fake, fake,
+                                                            fake, None, None)
+    assert call(smla.smla_topk_dims(4, 1, 0, 128, 2, 0)) == 1      # k = 0
+    assert call(smla.smla_topk_dims(4, 0, 64, 128, 2, 0)) == 1     # s_q = 0
+    assert call(smla.smla_topk_dims(4, 1, 64, 128, 2, 7)) == 2     # dtype
+    assert call(smla.smla_topk_dims(4, 1, 64, 100, 2, 0)) == 3     # row stride not 16 bytes
+    assert call(d, fake + 8) == 3                                  # misaligned scores
+    assert L.sparse_mla_topk_page_table(ctypes.byref(d), fake, None, fake, fake, None, None) == 1
+    assert call(smla.smla_topk_dims(0, 1, 64, 128, 2, 0)) == 0     # no rows: nothing to do

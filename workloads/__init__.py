@@ -230,6 +230,19 @@ def topk_lengths(b: int, s_q: int, topk: int, seed: int, device="cpu") -> torch.
     return lens.to(torch.int32).view(b, s_q).to(device)
 
 
+def index_scores(n_tok: int, ld: int, dtype=torch.bfloat16, seed: int = 0, device="cpu",
+                 levels: int = 0) -> torch.Tensor:
+    """[n_tok, ld] synthetic index scores, N(0, 1) rounded to ``dtype`` (bf16 rounding makes
+    ties common at any threshold); levels > 0 draws from that many integer values instead (a
+    tie-heavy row)."""
+    g = _gen(torch.device("cpu"), seed)
+    if levels > 0:
+        x = torch.randint(0, levels, (n_tok, ld), generator=g).float()
+    else:
+        x = torch.randn(n_tok, ld, generator=g)
+    return x.to(dtype).to(device)
+
+
 def to_numpy_inputs(wl: Workload):
     """(q as uint16 bf16 bits, kv uint8, indices int32) numpy arrays on the host."""
     q = wl.q.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
