@@ -4,19 +4,23 @@
 // section 5, step five).
 //
 // One CTA per query token (row).  Scores map to order-preserving unsigned keys (16-bit for
-// bf16, 32-bit for fp32) and the k-th largest key is found 8 bits at a time, most significant
-// first (a radix select):
-//   pass 1   histogram of the top 8 key bits over the valid prefix of the row;
+// bf16, 32-bit for fp32) and the k-th largest key is found a few bits at a time, most
+// significant first (a radix select):
+//   pass 1   histogram of the top 12 key bits over the valid prefix of the row;
 //   level 0  the threshold bin b is the one where the count of larger bins stops reaching k;
 //            a second pass over the row emits every element of a larger bin, keeps the
 //            positions of bin b as candidates in shared memory and builds the histogram of
-//            their next 8 bits;
-//   level l  the same on the candidates only, until every key bit is fixed; the elements left
-//            then all equal the k-th largest key and fill the remaining slots by a countdown.
+//            their next bits;
+//   level l  the same on the candidates only, until every key bit is fixed (bf16: 12 + 4
+//            bits, fp32: 12 + 10 + 10); the elements left then all equal the k-th largest key
+//            and fill the remaining slots by a countdown.
+// The pages' kernel starts with 8 bits; 12 bits (an eighth of a binade per bin) keep the
+// threshold bin of bell-shaped scores a few percent of the row instead of a quarter of it.
 // If bin b holds more candidates than shared memory, the next levels re-read the row and
-// filter it by the key prefix instead (slower, same result).  Elements are emitted as
-// block_table[req][u / 64] * 64 + u % 64 directly into the output row, in no particular
-// order; a row with at most k valid positions emits all of them and pads with -1.
+// filter it by the key prefix instead (slower, same result).  Emits and candidate pushes take
+// one shared atomic per warp.  Elements are emitted as block_table[req][u / 64] * 64 + u % 64
+// directly into the output row, in no particular order; a row with at most k valid positions
+// emits all of them and pads with -1.
 #include <cstdint>
 
 #include "../../include/sparse_mla.h"
@@ -26,8 +30,22 @@
 namespace smla {
 namespace {
 
-constexpr int TK_THREADS = 1024;
-constexpr int TK_CAP = 8192;  // candidate positions per buffer (two buffers)
+#ifndef SMLA_TOPK_THREADS
+#define SMLA_TOPK_THREADS 1024
+#endif
+#ifndef SMLA_TOPK_CAP
+#define SMLA_TOPK_CAP 8192
+#endif
+#ifndef SMLA_TOPK_UNROLL
+#define SMLA_TOPK_UNROLL 1
+#endif
+#ifndef SMLA_TOPK_MINB
+#define SMLA_TOPK_MINB 2
+#endif
+constexpr int TK_THREADS = SMLA_TOPK_THREADS;
+constexpr int TK_CAP = SMLA_TOPK_CAP;         // candidate positions per buffer (two buffers)
+constexpr int TK_UNROLL = SMLA_TOPK_UNROLL;   // 16-byte loads per thread in flight
+constexpr int TK_BINS = 4096;  // the widest level (12 bits)
 
 struct TopkParams {
   const void* scores;
@@ -38,27 +56,76 @@ struct TopkParams {
   int n_tok, s_q, k, ld, max_pages;
 };
 
+// Key bits resolved by each level, most significant first.
+template <bool kF32>
+__device__ __forceinline__ constexpr int level_bits(int l) {
+  return l == 0 ? 12 : (kF32 ? 10 : 4);
+}
+template <bool kF32>
+__device__ __forceinline__ constexpr int levels() {
+  return kF32 ? 3 : 2;
+}
+
 // Order-preserving keys: a larger score gives a larger unsigned key (negative values have
 // all their bits flipped, non-negative ones only the sign bit).
 template <bool kF32>
-__device__ __forceinline__ uint32_t key_at(const TopkParams& p, const void* row, int u) {
-  if (kF32) {
-    const uint32_t x = __float_as_uint(reinterpret_cast<const float*>(row)[u]);
-    return x ^ ((x >> 31) ? 0xFFFFFFFFu : 0x80000000u);
-  }
-  const uint32_t x = reinterpret_cast<const uint16_t*>(row)[u];
+__device__ __forceinline__ uint32_t to_key(uint32_t x) {
+  if (kF32) return x ^ ((x >> 31) ? 0xFFFFFFFFu : 0x80000000u);
   return x ^ ((x & 0x8000u) ? 0xFFFFu : 0x8000u);
+}
+template <bool kF32>
+__device__ __forceinline__ uint32_t key_at(const uint8_t* row, int u) {
+  if (kF32) return to_key<true>(__float_as_uint(reinterpret_cast<const float*>(row)[u]));
+  return to_key<false>(reinterpret_cast<const uint16_t*>(row)[u]);
+}
+// Element e of a 16-byte vector (4 fp32 or 8 bf16) as a key.
+template <bool kF32>
+__device__ __forceinline__ uint32_t vec_key(const uint4& w, int e) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  if (kF32) return to_key<true>(ws[e]);
+  return to_key<false>((ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
 }
 
 struct TopkShared {
-  uint32_t hist[256];
   uint32_t n_out, n_cand, ties, overflow, bad;
-  uint32_t bin, above;  // threshold bin of the current level and the count of larger bins
+  uint32_t bin, above;       // threshold bin of the current level and the count of larger bins
+  uint32_t warp_sum[32], warp_above[32];
 };
 
-__device__ __forceinline__ void emit(const TopkParams& p, TopkShared& sh, int row, int req,
-                                     int u) {
-  const uint32_t pos = atomicAdd(&sh.n_out, 1u);
+// Claims `take ? 1 : 0` consecutive slots of *counter for this lane with one atomic per warp;
+// returns this lane's slot (meaningful when take).
+__device__ __forceinline__ uint32_t warp_append(uint32_t* counter, bool take) {
+  const unsigned mask = __activemask();
+  const unsigned bal = __ballot_sync(mask, take);
+  if (bal == 0u) return 0u;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(bal) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
+  base = __shfl_sync(mask, base, leader);
+  return base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
+}
+
+// Reserves `n` consecutive slots of *counter for this lane (warp scan of the counts, one
+// atomic by the last active lane); returns this lane's first slot.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, uint32_t n) {
+  const unsigned mask = __activemask();
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(mask, incl, o);
+    if (lane >= o && ((mask >> (lane - o)) & 1u)) incl += v;
+  }
+  const int last = 31 - __clz(mask);
+  uint32_t base = 0;
+  if (lane == last && incl != 0u) base = atomicAdd(counter, incl);
+  base = __shfl_sync(mask, base, last);
+  return base + incl - n;
+}
+
+__device__ __forceinline__ void emit_at(const TopkParams& p, TopkShared& sh, int row, int req,
+                                        uint32_t pos, int u) {
   if (pos >= static_cast<uint32_t>(p.k)) return;
   const int pg = u >> 6;
   int32_t id = -1;
@@ -67,150 +134,269 @@ __device__ __forceinline__ void emit(const TopkParams& p, TopkShared& sh, int ro
   p.out[static_cast<size_t>(row) * p.k + pos] = id;
 }
 
-// Threshold of one level: the bin b whose suffix count (bins >= b) first reaches `need`,
-// and the count of the bins above it.  One warp; lane L owns bins 8 L .. 8 L + 7.
-__device__ __forceinline__ void find_threshold(TopkShared& sh, uint32_t need) {
-  const int lane = threadIdx.x & 31;
-  uint32_t c[8], local = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    c[i] = sh.hist[8 * lane + i];
-    local += c[i];
-  }
-  // count in the lanes above this one (bins above 8 lane + 7)
-  uint32_t incl = local;
+// Threshold of one level over hist[0, nbins): the bin b whose suffix count (bins >= b) first
+// reaches `need`, and the count of the bins above it.  Thread t owns bins [t * per, t * per +
+// per); a block-wide suffix scan (shuffles, then the 32 warp totals) finds the owner.
+__device__ void find_threshold(TopkShared& sh, const uint32_t* hist, int nbins, uint32_t need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nbins >= TK_THREADS ? nbins / TK_THREADS : 1;
+  const int b0 = tid * per;
+  uint32_t local = 0;
+  if (b0 < nbins)
+    for (int i = 0; i < per; ++i) local += hist[b0 + i];
+  uint32_t incl = local;  // sum over this and the higher lanes of the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t v = __shfl_down_sync(0xffffffffu, incl, o);
     if (lane + o < 32) incl += v;
   }
-  uint32_t above = incl - local;
-  if (above < need && incl >= need) {  // the threshold bin is in this lane
+  if (lane == 0) sh.warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < TK_THREADS / 32 ? sh.warp_sum[lane] : 0u;
+    uint32_t wi = w;
 #pragma unroll
-    for (int i = 7; i >= 0; --i) {
-      if (above + c[i] >= need) {
-        sh.bin = static_cast<uint32_t>(8 * lane + i);
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, wi, o);
+      if (lane + o < 32) wi += v;
+    }
+    sh.warp_above[lane] = wi - w;  // the warps above this one
+  }
+  __syncthreads();
+  incl += sh.warp_above[warp];
+  uint32_t above = incl - local;
+  if (b0 < nbins && above < need && incl >= need) {
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = hist[b0 + i];
+      if (above + c >= need) {
+        sh.bin = static_cast<uint32_t>(b0 + i);
         sh.above = above;
         break;
       }
-      above += c[i];
+      above += c;
     }
   }
+  __syncthreads();
 }
 
 template <bool kF32>
-__global__ void __launch_bounds__(TK_THREADS) topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const TopkParams p) {
   constexpr int kKeyBits = kF32 ? 32 : 16;
-  constexpr int kLevels = kKeyBits / 8;
   constexpr int kVec = kF32 ? 4 : 8;  // elements per 16-byte load
   extern __shared__ uint32_t tk_smem[];
   __shared__ TopkShared sh;
-  uint32_t* cand[2] = {tk_smem, tk_smem + TK_CAP};
+  uint32_t* hist = tk_smem;                  // [TK_BINS]
+  uint32_t* cand0 = tk_smem + TK_BINS;       // [TK_CAP]
+  uint32_t* cand1 = cand0 + TK_CAP;          // [TK_CAP]
   const int row = blockIdx.x, tid = threadIdx.x;
   const int req = row / p.s_q;
   int len = p.valid_len[row];
   len = len < 0 ? 0 : (len > p.ld ? p.ld : len);
   const uint8_t* rowp = static_cast<const uint8_t*>(p.scores) +
                         static_cast<size_t>(row) * p.ld * (kF32 ? 4 : 2);
-  if (tid == 0) {
-    sh.n_out = 0;
-    sh.n_cand = 0;
-    sh.ties = 0;
-    sh.overflow = 0;
-    sh.bad = 0;
-  }
   if (len <= p.k) {  // every valid position is selected
     for (int u = tid; u < p.k; u += TK_THREADS) {
       int32_t id = -1;
       if (u < len) {
         const int pg = u >> 6;
         if (pg < p.max_pages) id = p.table[static_cast<size_t>(req) * p.max_pages + pg] * 64 + (u & 63);
-        else atomicOr(p.status != nullptr ? p.status : &sh.bad, SMLA_DEV_TOPK_TABLE);
+        else if (p.status != nullptr) atomicOr(p.status, SMLA_DEV_TOPK_TABLE);
       }
       p.out[static_cast<size_t>(row) * p.k + u] = id;
     }
     return;
   }
-  for (int i = tid; i < 256; i += TK_THREADS) sh.hist[i] = 0;
-  __syncthreads();
-  // pass 1: top 8 key bits over the valid prefix, 16 bytes per load
+  if (tid == 0) {
+    sh.n_out = 0;
+    sh.n_cand = 0;
+    sh.ties = 0;
+    sh.overflow = 0;
+    sh.bad = 0;
+    sh.bin = 0;    // stays 0 when a threshold search finds no bin (fewer elements than asked)
+    sh.above = 0;
+  }
   const int nvec = len / kVec;
-  for (int v = tid; v < nvec; v += TK_THREADS) {
+  // Sampled pass: the 12-bit histogram of every 16th vector picks a boundary bin b_low that
+  // (from the sample) about 1.25 k + 256 elements reach; one full pass then keeps every element
+  // of bin b_low or above as a candidate, with the exact histogram of the candidates.  The top
+  // k are all among the candidates when there are at least k of them; with fewer, or more than
+  // the buffer holds, the exact method below runs on the whole row instead.
+  for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
+  __syncthreads();
+  for (int v = tid * 16; v < nvec; v += TK_THREADS * 16) {
     const uint4 w = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-      uint32_t key;
-      if (kF32) {
-        const uint32_t x = ws[e];
-        key = x ^ ((x >> 31) ? 0xFFFFFFFFu : 0x80000000u);
-      } else {
-        const uint32_t x = (ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-        key = x ^ ((x & 0x8000u) ? 0xFFFFu : 0x8000u);
+    for (int e = 0; e < kVec; ++e) atomicAdd(&hist[vec_key<kF32>(w, e) >> (kKeyBits - 12)], 1u);
+  }
+  __syncthreads();
+  find_threshold(sh, hist, 1 << 12, static_cast<uint32_t>((5 * p.k) / 64 + 16));
+  const uint32_t b_low = sh.above + hist[sh.bin] >= static_cast<uint32_t>((5 * p.k) / 64 + 16) ? sh.bin : 0u;
+  __syncthreads();
+  for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
+  __syncthreads();
+  // TK_UNROLL 16-byte loads per thread in flight, then the vectors in turn
+  for (int v0 = tid; v0 < nvec; v0 += TK_UNROLL * TK_THREADS) {
+    uint4 ws[TK_UNROLL];
+#pragma unroll
+    for (int j = 0; j < TK_UNROLL; ++j) {
+      const int v = v0 + j * TK_THREADS;
+      if (v < nvec) ws[j] = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
+    }
+#pragma unroll
+    for (int j = 0; j < TK_UNROLL; ++j) {
+      const int v = v0 + j * TK_THREADS;
+      if (v >= nvec) break;  // the lanes still going are a prefix of the warp
+      const uint4 w = ws[j];
+      uint32_t m_keep = 0;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e)
+        m_keep |= static_cast<uint32_t>((vec_key<kF32>(w, e) >> (kKeyBits - 12)) >= b_low) << e;
+      const unsigned mask = __activemask();
+      if (!__any_sync(mask, m_keep != 0u)) continue;
+      uint32_t slot = warp_reserve(&sh.n_cand, __popc(m_keep));
+      while (m_keep) {
+        const int e = __ffs(m_keep) - 1;
+        m_keep &= m_keep - 1u;
+        if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(v * kVec + e);
+        ++slot;
+        atomicAdd(&hist[vec_key<kF32>(w, e) >> (kKeyBits - 12)], 1u);
       }
-      atomicAdd(&sh.hist[key >> (kKeyBits - 8)], 1u);
     }
   }
-  for (int u = nvec * kVec + tid; u < len; u += TK_THREADS)
-    atomicAdd(&sh.hist[key_at<kF32>(p, rowp, u) >> (kKeyBits - 8)], 1u);
+  for (int u = nvec * kVec + tid; u < len; u += TK_THREADS) {
+    const uint32_t key = key_at<kF32>(rowp, u);
+    const bool keep = (key >> (kKeyBits - 12)) >= b_low;
+    const uint32_t slot = warp_append(&sh.n_cand, keep);
+    if (keep) {
+      if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(u);
+      atomicAdd(&hist[key >> (kKeyBits - 12)], 1u);
+    }
+  }
+  __syncthreads();
+  int src = 0;  // -1: the whole row (filtered by prefix); 0 / 1: a candidate buffer
+  if (sh.n_cand < static_cast<uint32_t>(p.k) || sh.n_cand > static_cast<uint32_t>(TK_CAP)) {
+    // the exact method on the whole row: the 12-bit histogram of every element
+    __syncthreads();
+    for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
+    __syncthreads();
+    for (int v = tid; v < nvec; v += TK_THREADS) {
+      const uint4 w = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) atomicAdd(&hist[vec_key<kF32>(w, e) >> (kKeyBits - 12)], 1u);
+    }
+    for (int u = nvec * kVec + tid; u < len; u += TK_THREADS)
+      atomicAdd(&hist[key_at<kF32>(rowp, u) >> (kKeyBits - 12)], 1u);
+    src = -1;
+  }
   __syncthreads();
   uint32_t need = static_cast<uint32_t>(p.k);
-  uint32_t prefix = 0;  // key bits fixed so far (the top 8 * level bits)
-  if (tid < 32) find_threshold(sh, need);
-  __syncthreads();
-  // Levels: at level l the threshold bin b of bits [kKeyBits - 8 (l + 1), kKeyBits - 8 l) is
-  // known; one pass over the level's elements emits the larger bins, keeps bin b (the next
-  // level's candidates) and builds the next level's histogram.
-  int src = -1;  // -1: the whole row (filtered by prefix); 0 / 1: a candidate buffer
-  for (int level = 0; level < kLevels; ++level) {
+  uint32_t prefix = 0;  // key bits fixed by the levels before this one
+  int consumed = 0;     // how many
+  find_threshold(sh, hist, 1 << 12, need);
+  for (int level = 0; level < levels<kF32>(); ++level) {
+    const int bits = level_bits<kF32>(level);
+    const int shift = kKeyBits - consumed - bits;
+    const bool last = level == levels<kF32>() - 1;
+    const int nbits = last ? 0 : level_bits<kF32>(level + 1);
     const uint32_t b = sh.bin;
-    const uint32_t above = sh.above;
-    const int shift = kKeyBits - 8 * (level + 1);
-    const bool last = level == kLevels - 1;
-    const uint32_t take = need - above;  // of bin b, this many are selected
+    const uint32_t take = need - sh.above;  // of bin b, this many are selected
+    const bool all_of_bin = take == hist[b];
     const uint32_t n_src = src < 0 ? 0u : sh.n_cand;
-    const bool all_of_bin = take == sh.hist[b];
     __syncthreads();
     if (tid == 0) sh.n_cand = 0;
-    for (int i = tid; i < 256; i += TK_THREADS) sh.hist[i] = 0;
+    if (!last && !all_of_bin)
+      for (int i = tid; i < (1 << nbits); i += TK_THREADS) hist[i] = 0;
     __syncthreads();
-    const int dst = src == 0 ? 1 : 0;
-    auto visit = [&](int u, uint32_t key) {
-      const uint32_t d = (key >> shift) & 0xFFu;
-      if (d > b) {
-        emit(p, sh, row, req, u);
-      } else if (d == b) {
-        if (last || all_of_bin) {
-          // every element of bin b is selected, or the keys are fully fixed: fill by countdown
-          if (all_of_bin || atomicAdd(&sh.ties, 1u) < take) emit(p, sh, row, req, u);
-        } else {
-          const uint32_t slot = atomicAdd(&sh.n_cand, 1u);
-          if (slot < TK_CAP) cand[dst][slot] = static_cast<uint32_t>(u);
+    uint32_t* dst = src == 0 ? cand1 : cand0;
+    const uint32_t* srcb = src == 0 ? cand0 : cand1;
+    // one element: emit it (larger bin, or bin b when all of it or, at the last level, a tie
+    // within the count), or keep it as a candidate of the next level
+    auto visit = [&](bool in, int u, uint32_t key) {
+      const uint32_t d = (key >> shift) & ((1u << bits) - 1u);
+      bool out = in && d > b;
+      const bool eq = in && d == b;
+      bool keep = false;
+      if (last || all_of_bin) {
+        bool tie_ok = eq;
+        if (!all_of_bin) {  // every lane takes part in the count (it is a warp collective)
+          const uint32_t t = warp_append(&sh.ties, eq);
+          tie_ok = eq && t < take;
+        }
+        out = out || tie_ok;
+      } else {
+        keep = eq;
+      }
+      const uint32_t pos = warp_append(&sh.n_out, out);
+      if (out) emit_at(p, sh, row, req, pos, u);
+      if (!last && !all_of_bin) {
+        const uint32_t slot = warp_append(&sh.n_cand, keep);
+        if (keep) {
+          if (slot < TK_CAP) dst[slot] = static_cast<uint32_t>(u);
           else sh.overflow = 1u;
-          atomicAdd(&sh.hist[(key >> (shift - 8)) & 0xFFu], 1u);
+          atomicAdd(&hist[(key >> (shift - nbits)) & ((1u << nbits) - 1u)], 1u);
         }
       }
     };
-    if (src < 0) {
+    if (src < 0 && consumed == 0 && !last && !all_of_bin) {
+      // level 0 over the whole row (the common case): per 16-byte vector each lane marks its
+      // larger-bin and bin-b elements in two bit masks, and one warp scan per mask reserves
+      // their output and candidate slots
+      for (int v = tid; v < nvec; v += TK_THREADS) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
+        uint32_t m_out = 0, m_keep = 0;
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const uint32_t d = vec_key<kF32>(w, e) >> shift;
+          m_out |= static_cast<uint32_t>(d > b) << e;
+          m_keep |= static_cast<uint32_t>(d == b) << e;
+        }
+        const unsigned mask = __activemask();
+        if (!__any_sync(mask, (m_out | m_keep) != 0u)) continue;
+        uint32_t pos = warp_reserve(&sh.n_out, __popc(m_out));
+        uint32_t slot = warp_reserve(&sh.n_cand, __popc(m_keep));
+        while (m_out) {
+          const int e = __ffs(m_out) - 1;
+          m_out &= m_out - 1u;
+          emit_at(p, sh, row, req, pos++, v * kVec + e);
+        }
+        while (m_keep) {
+          const int e = __ffs(m_keep) - 1;
+          m_keep &= m_keep - 1u;
+          if (slot < TK_CAP) dst[slot] = static_cast<uint32_t>(v * kVec + e);
+          else sh.overflow = 1u;
+          ++slot;
+          atomicAdd(&hist[(vec_key<kF32>(w, e) >> (shift - nbits)) & ((1u << nbits) - 1u)], 1u);
+        }
+      }
+      for (int u = nvec * kVec + tid; u < len; u += TK_THREADS) visit(true, u, key_at<kF32>(rowp, u));
+    } else if (src < 0) {
       // the whole row: elements whose fixed key bits match the prefix
-      const int pshift = kKeyBits - 8 * level;  // bits above this level
-      for (int u = tid; u < len; u += TK_THREADS) {
-        const uint32_t key = key_at<kF32>(p, rowp, u);
-        if (level == 0 || (key >> pshift) == prefix) visit(u, key);
+      const int pshift = kKeyBits - consumed;
+      for (int v = tid; v < nvec; v += TK_THREADS) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const uint32_t key = vec_key<kF32>(w, e);
+          visit(consumed == 0 || (key >> pshift) == prefix, v * kVec + e, key);
+        }
+      }
+      for (int u = nvec * kVec + tid; u < len; u += TK_THREADS) {
+        const uint32_t key = key_at<kF32>(rowp, u);
+        visit(consumed == 0 || (key >> pshift) == prefix, u, key);
       }
     } else {
       for (uint32_t i = tid; i < n_src; i += TK_THREADS) {
-        const int u = static_cast<int>(cand[src][i]);
-        visit(u, key_at<kF32>(p, rowp, u));
+        const int u = static_cast<int>(srcb[i]);
+        visit(true, u, key_at<kF32>(rowp, u));
       }
     }
     __syncthreads();
     if (last || all_of_bin) break;
-    prefix = (prefix << 8) | b;
+    prefix = (prefix << bits) | b;
+    consumed += bits;
     need = take;
-    src = sh.overflow ? -1 : dst;  // after an overflow the next levels re-read the row
-    if (tid < 32) find_threshold(sh, need);
-    __syncthreads();
+    src = sh.overflow ? -1 : (src == 0 ? 1 : 0);  // after an overflow the levels re-read the row
+    find_threshold(sh, hist, 1 << nbits, need);
   }
   if (tid == 0 && sh.bad && p.status != nullptr) atomicOr(p.status, SMLA_DEV_TOPK_TABLE);
 }
@@ -221,7 +407,7 @@ cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
                         const int32_t* table, int32_t* out, uint32_t* status, int n_tok, int s_q,
                         int k, int ld, int max_pages, cudaStream_t stream) {
   TopkParams p{scores, valid_len, table, out, status, n_tok, s_q, k, ld, max_pages};
-  const size_t smem = 2 * TK_CAP * sizeof(uint32_t);
+  const size_t smem = (TK_BINS + 2 * TK_CAP) * sizeof(uint32_t);
   void (*kernel)(TopkParams) = fp32 ? topk_kernel<true> : topk_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
