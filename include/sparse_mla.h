@@ -183,6 +183,11 @@ smla_status sparse_mla_combine(const smla_dims* dims, int num_sms, const void* s
  *                normalised by their own exp-sum, so they are bounded by the largest value
  *                element).  Results stay within the library's tolerance but differ in the
  *                last bits from the fp32 path; the workspace size is unchanged.
+ *   test_stall   test hook for the failure path, 0 in use: nonzero makes the MMA issuer of
+ *                every partition's score CTA wait on a barrier that nothing arrives at.  Each
+ *                waiting role gives up after its bounded wait (about 1 s), the kernel returns,
+ *                the device status word gets SMLA_DEV_TIMEOUT and word 1 the first wait that
+ *                ran out; the outputs of that call are not valid and the context stays usable.
  * The same options must be given to sparse_mla_decode_fwd_ex and sparse_mla_combine_ex of
  * one problem: the decode pass applies the sink to unsplit rows, the combine to split rows,
  * and both must agree on the partials' type.
@@ -194,6 +199,7 @@ typedef struct {
   const void* extra_kv_cache;
   const int32_t* extra_indices;
   const int32_t* extra_topk_length;
+  int32_t test_stall;
 } smla_decode_opts;
 
 /* sparse_mla_decode_fwd with decode options (opts may be NULL: then identical to it).

@@ -64,7 +64,8 @@ class smla_decode_opts(ctypes.Structure):
     optional lengths (int32 [b, s_q])."""
     _fields_ = [("attn_sink", ctypes.c_void_p), ("topk_length", ctypes.c_void_p),
                 ("partials_bf16", ctypes.c_int32), ("extra_kv_cache", ctypes.c_void_p),
-                ("extra_indices", ctypes.c_void_p), ("extra_topk_length", ctypes.c_void_p)]
+                ("extra_indices", ctypes.c_void_p), ("extra_topk_length", ctypes.c_void_p),
+                ("test_stall", ctypes.c_int32)]
 
 
 class smla_topk_dims(ctypes.Structure):

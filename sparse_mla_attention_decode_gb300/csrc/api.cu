@@ -234,6 +234,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.attn_sink = opts != nullptr ? opts->attn_sink : nullptr;
   p.topk_length = opts != nullptr ? opts->topk_length : nullptr;
   p.partials_bf16 = opts != nullptr && opts->partials_bf16 != 0 ? 1 : 0;
+  p.test_stall = opts != nullptr && opts->test_stall != 0 ? 1 : 0;
   p.b = dims->b;
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;

@@ -79,6 +79,7 @@ enum Bar {
   B_OSTAGE = B_QREAD + 1,           // [8] 128 epilogue threads staged one output box (O-CTA)
   B_OFREE = B_OSTAGE + 8,           // the stores have read the staging tiles (O-CTA)
   B_LAST = B_OFREE + 1,             // one-shot commit after the partition's final PV (O-CTA)
+  B_NEVER = B_LAST + 1,             // nothing arrives here (the test_stall hook waits on it)
   NUM_BARS
 };
 constexpr int OFF_BARS = OFF_MISC;
@@ -381,7 +382,12 @@ out:
 
 // ---------------------------------------------------------------------------------------
 // S-CTA MMA warp (one lane): S[buf] = Q K^T for every block (36 MMAs of K = 16).
-__device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase) {
+__device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bool stall) {
+  // test hook: a wait that nothing ends, so every role runs into its bounded wait
+  if (stall) {
+    c.wait(B_NEVER, 0);
+    return;
+  }
   uint32_t g = 0, item = 0;
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     if (!c.wait(B_Q_FULL, item & 1)) return;
@@ -892,6 +898,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     for (int b = 0; b < 8; ++b) mbar_init(c.bar(B_OSTAGE + b), 128);
     mbar_init(c.bar(B_OFREE), 1);
     mbar_init(c.bar(B_LAST), 1);
+    mbar_init(c.bar(B_NEVER), 1);
 
     mbar_init(c.bar(B_O_FULL), 1);
     mbar_init(c.bar(B_O_EMPTY), 128);
@@ -931,7 +938,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       else role_dequant<false, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
     } else if (warp == 12) {
       if (lane == 0) {
-        if (scores) role_mma_scores(c, pl, tbase);
+        if (scores) role_mma_scores(c, pl, tbase, p.test_stall != 0);
         else role_mma_values(c, pl, tbase);
         mma_commit(c.bar(B_DRAIN));  // every issued MMA has finished before TMEM is freed
         c.drain(B_DRAIN, 0);

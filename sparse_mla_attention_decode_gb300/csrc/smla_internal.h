@@ -77,6 +77,7 @@ struct DecodeParams {
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
   int store32;              // out and the workspace are 32-byte aligned (256-bit stores)
   int partials_bf16;        // split partials of O stored as bf16 rows (else fp32)
+  int test_stall;           // failure-path test hook (see smla_decode_opts)
 };
 
 struct CombineParams {

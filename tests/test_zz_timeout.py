@@ -1,0 +1,58 @@
+"""The failure path on the GPU without a fault: the test_stall hook makes every partition's
+MMA issuer wait on a barrier that nothing arrives at.  Every waiting role gives up after its
+bounded wait, the kernel returns, the device status word reports SMLA_DEV_TIMEOUT and records
+the first wait that ran out, and the context stays usable: the next call is correct and
+clean.  (Runs last: it takes about a second of wall time.)"""
+
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mla_attention_decode_gb300 as smla
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable(cuda_ok):
+    dev = torch.device("cuda:0")
+    wl = workloads.small(b=3, h_q=128, topk=256, ctx=1024, device=dev, seed=61)
+    op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
+                              wl.kv.shape[0], device=dev, num_sms=16)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    out = torch.empty(3, 1, 128, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(3, 128, 1, dtype=torch.float32, device=dev)
+    opts = smla.smla_decode_opts()
+    opts.test_stall = 1
+    smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+    t0 = time.perf_counter()
+    smla.sparse_mla_decode_fwd_ex(op.dims, op.num_sms, wl.q.data_ptr(), wl.kv.data_ptr(),
+                                  wl.indices.data_ptr(), wl.sm_scale, opts, op.sched.data_ptr(),
+                                  op.workspace.data_ptr(), op.accum_bytes, out.data_ptr(),
+                                  lse.data_ptr(), st)
+    smla.sparse_mla_combine_ex(op.dims, op.num_sms, opts, op.sched.data_ptr(),
+                               op.workspace.data_ptr(), op.accum_bytes, out.data_ptr(),
+                               lse.data_ptr(), st)
+    rc, word = smla.sparse_mla_read_device_status(op.dims, op.num_sms, op.sched.data_ptr(), st)
+    waited = time.perf_counter() - t0
+    assert rc == smla.SMLA_ERR_TIMEOUT and word & smla.SMLA_DEV_TIMEOUT
+    assert waited > 0.5  # the bounded waits (one second) ran out; nothing returned early
+    # status word 1: the first wait that ran out (marker bit, CTA rank, role, barrier, parity)
+    meta, pre = op.plan()
+    parts = meta.shape[0]
+    status_off = ((parts * 32 + (3 + 1) * 4) + 15) // 16 * 16
+    words = op.sched.cpu()[status_off:status_off + 8].view(torch.int32)
+    assert int(words[1]) & 0x80000000 == 0x80000000 or int(words[1]) < 0
+    # the context is usable: the same problem again, normally
+    out2, lse2 = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale)
+    torch.cuda.synchronize(dev)
+    assert op.device_status() == 0
+    q, kv, idx = workloads.to_numpy_inputs(wl)
+    ro, rl = oracle.sparse_mla_decode_full(q, kv, idx, wl.sm_scale)
+    gu.compare(out2.double().cpu().numpy().reshape(-1, 128, 512),
+               lse2.double().cpu().numpy().transpose(0, 2, 1).reshape(-1, 128),
+               ro.reshape(-1, 128, 512), rl.transpose(0, 2, 1).reshape(-1, 128), "after a timeout")
