@@ -304,6 +304,46 @@ smla_status sparse_mla_topk_page_table(const smla_topk_dims* dims, const void* s
                                        const int32_t* valid_len, const int32_t* block_table,
                                        int32_t* out_indices, uint32_t* status, void* stream);
 
+/*
+ * sparse_mla_indexer_scores -- the lightning-indexer scores the top-k selects from ("FlashMLA 与
+ * DSA", section 4.1: I[t, s] = sum_j w[t, j] ReLU(q[t, j] . k[s]) with e4m3 q and k and one key
+ * per cached token shared by the 64 heads; section 5.3: the paged cache layout and the key
+ * scale applied after the head sum; "sparse-attention co-design", section 5, steps one to
+ * four: the query scale folded into w).  For every query token t and position s <
+ * valid_len[t]:
+ *     scores[t][s] = k_scale[s] * sum_{j < 64} w[t][j] * max(q8[t][j] . k8[s], 0)
+ * computed with e4m3 x e4m3 tensor-core MMAs accumulated in fp32.
+ *   dims->n_tok      query tokens; token t belongs to request t / s_q (n_tok % s_q == 0)
+ *   dims->s_q        query tokens per request
+ *   dims->heads      64;  dims->dim  128
+ *   dims->max_pages  columns of the page table;  dims->num_pages  pages in the cache
+ *   dims->ld         row stride of scores (valid_len is clamped to it)
+ *   q8               device uint8 [n_tok][64][128] e4m3 codes, 16-byte aligned
+ *   weights          device fp32 [n_tok][64] (the query scales and normalisations folded in)
+ *   k_cache          device uint8 [num_pages][8448]: 64 x 128 e4m3 codes of a page's tokens,
+ *                    then their 64 fp32 scales; 16-byte aligned
+ *   block_table      device int32 [n_tok / s_q][max_pages]
+ *   valid_len        device int32 [n_tok]
+ *   scores           device fp32 [n_tok][ld] (written for s < min(valid_len[t], ld,
+ *                    max_pages * 64) only); a page id outside [0, num_pages) scores 0
+ *   status           optional device uint32 word (SMLA_DEV_TIMEOUT if a wait ran out)
+ * num_sms <= 0 means all SMs of the current device.  Asynchronous on stream.  Errors:
+ * SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_ALIGNMENT, SMLA_ERR_CUDA.
+ */
+typedef struct {
+  int32_t n_tok;
+  int32_t s_q;
+  int32_t heads;
+  int32_t dim;
+  int32_t max_pages;
+  int32_t ld;
+  int64_t num_pages;
+} smla_indexer_dims;
+smla_status sparse_mla_indexer_scores(const smla_indexer_dims* dims, int num_sms, const void* q8,
+                                      const float* weights, const void* k_cache,
+                                      const int32_t* block_table, const int32_t* valid_len,
+                                      float* scores, uint32_t* status, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* sparse_mla_status_string(smla_status status);
 

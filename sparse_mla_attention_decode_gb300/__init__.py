@@ -23,6 +23,7 @@ __all__ = [
     "smla_decode_opts", "sparse_mla_decode_fwd_ex", "sparse_mla_combine_ex",
     "sparse_mla_plan_has_splits", "smla_topk_dims", "sparse_mla_topk_page_table",
     "topk_page_table", "SMLA_SCORES_BF16", "SMLA_SCORES_FP32",
+    "smla_indexer_dims", "sparse_mla_indexer_scores", "indexer_scores",
     "SparseMLADecode", "dims_for",
 ]
 
@@ -39,7 +40,8 @@ SMLA_SCORES_BF16, SMLA_SCORES_FP32 = 0, 1
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
             "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
-            "sparse_mla_combine_ex", "sparse_mla_plan_has_splits", "sparse_mla_topk_page_table"]
+            "sparse_mla_combine_ex", "sparse_mla_plan_has_splits", "sparse_mla_topk_page_table",
+            "sparse_mla_indexer_scores"]
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -71,6 +73,12 @@ class smla_decode_opts(ctypes.Structure):
 class smla_topk_dims(ctypes.Structure):
     _fields_ = [("n_tok", ctypes.c_int32), ("s_q", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("ld", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class smla_indexer_dims(ctypes.Structure):
+    _fields_ = [("n_tok", ctypes.c_int32), ("s_q", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("dim", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("ld", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -106,6 +114,8 @@ def lib():
                                                 vp, vp, sz, vp, vp, vp]
             L.sparse_mla_plan_has_splits.argtypes = [P(smla_dims), ctypes.c_int, P(ctypes.c_int)]
             L.sparse_mla_topk_page_table.argtypes = [P(smla_topk_dims), vp, vp, vp, vp, vp, vp]
+            L.sparse_mla_indexer_scores.argtypes = [P(smla_indexer_dims), ctypes.c_int, vp, vp, vp,
+                                                    vp, vp, vp, vp, vp]
             L.sparse_mla_status_string.argtypes = [ctypes.c_int]
             L.sparse_mla_status_string.restype = ctypes.c_char_p
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
@@ -237,6 +247,37 @@ def topk_page_table(scores, valid_len, block_table, s_q: int, k: int, out=None, 
     st = (stream if stream is not None else torch.cuda.current_stream(scores.device)).cuda_stream
     sparse_mla_topk_page_table(d, scores.data_ptr(), valid_len.data_ptr(), block_table.data_ptr(),
                                out.data_ptr(), status.data_ptr() if status is not None else 0, st)
+    return out
+
+
+def sparse_mla_indexer_scores(dims: smla_indexer_dims, num_sms: int, q8: int, weights: int,
+                              k_cache: int, block_table: int, valid_len: int, scores: int,
+                              status: int = 0, stream: int = 0) -> None:
+    _check(lib().sparse_mla_indexer_scores(ctypes.byref(dims), int(num_sms), q8, weights, k_cache,
+                                           block_table, valid_len, scores, status or None,
+                                           stream),
+           "sparse_mla_indexer_scores")
+
+
+def indexer_scores(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: int, out=None,
+                   status=None, num_sms: int = 0, stream=None):
+    """Indexer scores fp32 [n_tok, ld] (written for s < valid_len[t]) from e4m3 codes q8
+    (uint8 [n_tok, 64, 128]), fp32 weights [n_tok, 64], the paged key cache (uint8
+    [num_pages, 8448]) and the page table (int32 [n_tok / s_q, max_pages])."""
+    import torch
+    for name, t, dt in (("q8", q8, torch.uint8), ("weights", weights, torch.float32),
+                        ("k_cache", k_cache, torch.uint8), ("block_table", block_table, torch.int32),
+                        ("valid_len", valid_len, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor")
+    n_tok = q8.shape[0]
+    if out is None:
+        out = torch.empty(n_tok, ld, dtype=torch.float32, device=q8.device)
+    d = smla_indexer_dims(n_tok, s_q, 64, 128, block_table.shape[1], ld, k_cache.shape[0])
+    st = (stream if stream is not None else torch.cuda.current_stream(q8.device)).cuda_stream
+    sparse_mla_indexer_scores(d, num_sms, q8.data_ptr(), weights.data_ptr(), k_cache.data_ptr(),
+                              block_table.data_ptr(), valid_len.data_ptr(), out.data_ptr(),
+                              status.data_ptr() if status is not None else 0, st)
     return out
 
 

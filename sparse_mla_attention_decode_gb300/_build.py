@@ -13,7 +13,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsparse_mla.so")
-SOURCES = ["api.cu", "decode_fwd.cu", "sched_combine.cu", "static_scratch.cu", "topk.cu"]
+SOURCES = ["api.cu", "decode_fwd.cu", "sched_combine.cu", "static_scratch.cu", "topk.cu",
+           "indexer.cu"]
 HEADERS = ["ptx.cuh", "smla_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -121,6 +121,23 @@ bool smla::encode_rows_map(CUtensorMap* map, const void* base, bool fp32, int64_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool smla::encode_bytes_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t bx[3], elem[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank),
+             const_cast<void*>(base), d, st, bx, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 extern "C" {
 
 const char* sparse_mla_version(void) { return "sparse_mla 0.1 sm_103a"; }
@@ -313,6 +330,59 @@ smla_status sparse_mla_topk_page_table(const smla_topk_dims* d, const void* scor
   return cuda_status(launch_topk(scores, d->dtype == SMLA_SCORES_FP32, valid_len, block_table,
                                  out_indices, status, d->n_tok, d->s_q, d->topk, d->ld,
                                  d->max_pages, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status sparse_mla_indexer_scores(const smla_indexer_dims* d, int num_sms, const void* q8,
+                                      const float* weights, const void* k_cache,
+                                      const int32_t* block_table, const int32_t* valid_len,
+                                      float* scores, uint32_t* status, void* stream) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->n_tok < 0 || d->s_q < 1 || d->ld < 0 || d->max_pages < 0 || d->num_pages < 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->heads != 64 || d->dim != 128) return SMLA_ERR_UNSUPPORTED;
+  if (d->n_tok % d->s_q != 0) return SMLA_ERR_INVALID_ARG;
+  if (d->n_tok == 0 || d->ld == 0) return SMLA_OK;
+  if (!q8 || !weights || !block_table || !valid_len || !scores || (d->num_pages > 0 && !k_cache))
+    return SMLA_ERR_INVALID_ARG;
+  if (!aligned(q8, 16) || !aligned(k_cache, 16) || !aligned(weights, 4) ||
+      !aligned(block_table, 4) || !aligned(valid_len, 4) || !aligned(scores, 4) ||
+      !aligned(status, 4))
+    return SMLA_ERR_ALIGNMENT;
+  if (static_cast<int64_t>(d->n_tok) * 64 > INT32_MAX || d->num_pages > INT32_MAX ||
+      static_cast<int64_t>(d->n_tok) * d->ld > (int64_t(1) << 40))
+    return SMLA_ERR_UNSUPPORTED;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return SMLA_ERR_CUDA;
+    }
+  }
+  IndexerLaunch L;
+  const int G = d->s_q < 4 ? d->s_q : 4;
+  const uint64_t kd[3] = {128, 64, static_cast<uint64_t>(d->num_pages > 0 ? d->num_pages : 1)};
+  const uint64_t ks[2] = {128, 8448};
+  const uint32_t kb[3] = {128, 64, 1};
+  const uint64_t qd[2] = {128, static_cast<uint64_t>(d->n_tok) * 64};
+  const uint64_t qs[1] = {128};
+  const uint32_t qb[2] = {128, static_cast<uint32_t>(64 * G)};
+  const void* kbase = d->num_pages > 0 ? k_cache : q8;  // any valid address when there is no page
+  if (!encode_bytes_map(&L.k_map, kbase, 3, kd, ks, kb) || !encode_bytes_map(&L.q_map, q8, 2, qd, qs, qb))
+    return SMLA_ERR_CUDA;
+  L.w = weights;
+  L.table = block_table;
+  L.valid_len = valid_len;
+  L.cache = static_cast<const uint8_t*>(k_cache);
+  L.out = scores;
+  L.status = status;
+  L.n_tok = d->n_tok;
+  L.s_q = d->s_q;
+  L.max_pages = d->max_pages;
+  L.ld = d->ld;
+  L.num_sms = num_sms;
+  L.num_pages = d->num_pages;
+  return cuda_status(launch_indexer(L, static_cast<cudaStream_t>(stream)));
 }
 
 smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits) {

@@ -191,3 +191,14 @@ def test_topk_argument_checks(L):
     assert call(d, fake + 8) == 3                                  # misaligned scores
     assert L.sparse_mla_topk_page_table(ctypes.byref(d), fake, None, fake, fake, None, None) == 1
     assert call(smla.smla_topk_dims(0, 1, 64, 128, 2, 0)) == 0     # no rows: nothing to do
+
+
+def test_indexer_argument_checks(L):
+    fake = 0x10000
+    call = lambda d, q=fake: L.sparse_mla_indexer_scores(ctypes.byref(d), 152, q, fake, fake,
+                                                         fake, fake, fake, None, None)
+    assert call(smla.smla_indexer_dims(4, 1, 32, 128, 8, 512, 16)) == 2   # heads
+    assert call(smla.smla_indexer_dims(4, 1, 64, 64, 8, 512, 16)) == 2    # dim
+    assert call(smla.smla_indexer_dims(5, 2, 64, 128, 8, 512, 16)) == 1   # n_tok % s_q
+    assert call(smla.smla_indexer_dims(4, 1, 64, 128, 8, 512, 16), fake + 4) == 3  # q8 alignment
+    assert call(smla.smla_indexer_dims(0, 1, 64, 128, 8, 512, 16)) == 0   # nothing to do

@@ -243,6 +243,34 @@ def index_scores(n_tok: int, ld: int, dtype=torch.bfloat16, seed: int = 0, devic
     return x.to(dtype).to(device)
 
 
+def e4m3_codes(shape, seed: int, device="cpu", scale: float = 1.0) -> torch.Tensor:
+    """uint8 e4m3 codes of N(0, scale^2) values (saturated at +-448; never the NaN codes)."""
+    g = _gen(torch.device("cpu"), seed)
+    x = (torch.randn(shape, generator=g) * scale).clamp_(-E4M3_MAX, E4M3_MAX)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).to(device)
+
+
+def indexer_cache(num_pages: int, seed: int, device="cpu") -> torch.Tensor:
+    """uint8 [num_pages, 8448] indexer key pages: 64 x 128 e4m3 codes of N(0, 1) keys, then 64
+    fp32 per-token scales uniform on [0.5, 1.5] / 16."""
+    g = _gen(torch.device("cpu"), seed)
+    codes = e4m3_codes((num_pages, 64 * 128), seed + 1)
+    scales = (torch.rand(num_pages, 64, generator=g) + 0.5) / 16.0
+    page = torch.empty(num_pages, 64 * 128 + 256, dtype=torch.uint8)
+    page[:, : 64 * 128] = codes
+    page[:, 64 * 128:] = scales.float().contiguous().view(torch.uint8).view(num_pages, 256)
+    return page.to(device)
+
+
+def indexer_queries(n_tok: int, seed: int, device="cpu"):
+    """(q8 uint8 [n_tok, 64, 128] e4m3 codes of N(0, 1) queries, weights fp32 [n_tok, 64]
+    uniform on [-1, 1] / 8: signed, as the head weights are not a softmax)."""
+    g = _gen(torch.device("cpu"), seed)
+    q8 = e4m3_codes((n_tok, 64, 128), seed + 2)
+    w = (torch.rand(n_tok, 64, generator=g) * 2 - 1) / 8
+    return q8.to(device), w.float().to(device)
+
+
 def to_numpy_inputs(wl: Workload):
     """(q as uint16 bf16 bits, kv uint8, indices int32) numpy arrays on the host."""
     q = wl.q.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
