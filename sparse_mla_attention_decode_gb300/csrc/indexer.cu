@@ -13,9 +13,10 @@
 // reduction), and the [tokens x heads] products never leave the SM.
 //
 // Work item = (query group of G <= 4 tokens of one request, chunk of up to 16 key tiles); the
-// CTAs walk the items with a grid stride.  Warps 0-3: epilogue (thread = TMEM lane = token);
-// warp 4: TMA producer (Q once per item, two page boxes per key tile, four stages); warp 5:
-// MMA issuer (two TMEM accumulators of 256 columns).  Every wait is bounded (a second), after
+// CTAs walk the items with a grid stride.  Warps 0-7: epilogue, two warpgroups (thread = TMEM
+// lane = token; the even and the odd query tokens of the group); warp 8: TMA producer (Q once
+// per item into one of two buffers, two page boxes per key tile, six stages); warp 9: MMA issuer (two TMEM
+// accumulators of 256 columns).  Every wait is bounded (a second), after
 // which the CTA raises SMLA_DEV_TIMEOUT and its roles leave.
 #include <cstdint>
 
@@ -26,26 +27,29 @@
 namespace smla {
 namespace {
 
-constexpr int IX_THREADS = 192;
-constexpr int IX_STAGES = 4;
+constexpr int IX_THREADS = 320;  // warps 0-7 epilogue, 8 TMA producer, 9 MMA issuer
+constexpr int IX_STAGES = 6;
 constexpr int IX_TILE = 128;          // cached tokens per key tile (two pages)
 constexpr int IX_CHUNK = 16;          // key tiles per work item
 constexpr int IX_PAGE_BYTES = 8448;   // 64 x 128 codes + 64 x 4 scale bytes
 constexpr int IX_STAGE_BYTES = IX_TILE * 128;
 constexpr int IX_Q_BYTES = 256 * 128;
 constexpr int IX_OFF_Q = IX_STAGES * IX_STAGE_BYTES;
-constexpr int IX_OFF_BARS = IX_OFF_Q + IX_Q_BYTES;
+constexpr int IX_OFF_BARS = IX_OFF_Q + 2 * IX_Q_BYTES;  // two Q buffers (items alternate)
 enum IxBar {
-  IB_K_FULL = 0,                 // [4] expect-tx + the tile's bytes
-  IB_K_EMPTY = IB_K_FULL + 4,    // [4] commit after the tile's MMAs
-  IB_D_FULL = IB_K_EMPTY + 4,    // [2] commit after the tile's MMAs
-  IB_D_EMPTY = IB_D_FULL + 2,    // [2] 128 epilogue threads
-  IB_Q_FULL = IB_D_EMPTY + 2,    // expect-tx + Q's bytes
-  IB_Q_FREE = IB_Q_FULL + 1,     // commit after an item's last MMAs
-  IB_DRAIN = IB_Q_FREE + 1,
+  IB_K_FULL = 0,                          // [stages] expect-tx + the tile's bytes
+  IB_K_EMPTY = IB_K_FULL + IX_STAGES,     // [stages] commit after the tile's MMAs
+  IB_D_FULL = IB_K_EMPTY + IX_STAGES,     // [2] commit after the tile's MMAs
+  IB_D_EMPTY = IB_D_FULL + 2,             // [2] 256 epilogue threads
+  IB_Q_FULL = IB_D_EMPTY + 2,             // [2] expect-tx + Q's bytes
+  IB_Q_FREE = IB_Q_FULL + 2,              // [2] commit after an item's last MMAs
+  IB_DRAIN = IB_Q_FREE + 2,
   IB_COUNT
 };
-constexpr int IX_OFF_MISC = IX_OFF_BARS + IB_COUNT * 8;
+// [8 warps][256] head weights, 128-byte aligned (read as float4)
+constexpr int IX_OFF_W = (IX_OFF_BARS + IB_COUNT * 8 + 127) & ~127;
+static_assert(IX_OFF_W % 16 == 0, "float4 weight reads");
+constexpr int IX_OFF_MISC = IX_OFF_W + 8 * 256 * 4;
 // + TMEM slot, abort flag, alignment slack; at least 116 KB so that one CTA holds an SM (each
 // CTA allocates all 512 tensor-memory columns)
 constexpr int IX_SMEM_USED = IX_OFF_MISC + 32 + 1024;
@@ -121,9 +125,10 @@ __device__ void ix_producer(const IndexerParams& p, const IxCtx& c) {
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
     const IxItem it = item_of(p, item);
     if (it.tile0 >= it.tile1) continue;
-    if (n > 0 && !c.wait(IB_Q_FREE, (n - 1) & 1)) return;  // the previous item's MMAs are done
-    mbar_arrive_expect_tx(c.bar(IB_Q_FULL), static_cast<uint32_t>(p.G) * 64 * 128);
-    tma_load_2d(c.sbase + IX_OFF_Q, &p.q_map, 0, it.t0 * 64, c.bar(IB_Q_FULL));
+    const uint32_t qb = n & 1;  // the item two back used this Q buffer: its MMAs are done
+    if (n >= 2 && !c.wait(IB_Q_FREE + qb, ((n >> 1) - 1) & 1)) return;
+    mbar_arrive_expect_tx(c.bar(IB_Q_FULL + qb), static_cast<uint32_t>(p.G) * 64 * 128);
+    tma_load_2d(c.sbase + IX_OFF_Q + qb * IX_Q_BYTES, &p.q_map, 0, it.t0 * 64, c.bar(IB_Q_FULL + qb));
     const int pages = (it.maxlen + 63) / 64;
     const int32_t* row = p.table + static_cast<size_t>(it.req) * p.max_pages;
     for (int tile = it.tile0; tile < it.tile1; ++tile, ++gt) {
@@ -146,8 +151,9 @@ __device__ void ix_mma(const IndexerParams& p, const IxCtx& c, uint32_t tbase) {
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
     const IxItem it = item_of(p, item);
     if (it.tile0 >= it.tile1) continue;
-    if (!c.wait(IB_Q_FULL, n & 1)) return;
-    const uint64_t bdesc = umma_desc(c.sbase + IX_OFF_Q, 16, 1024, 2);
+    const uint32_t qb = n & 1;
+    if (!c.wait(IB_Q_FULL + qb, (n >> 1) & 1)) return;
+    const uint64_t bdesc = umma_desc(c.sbase + IX_OFF_Q + qb * IX_Q_BYTES, 16, 1024, 2);
     for (int tile = it.tile0; tile < it.tile1; ++tile, ++gt) {
       const uint32_t st = gt % IX_STAGES, db = gt & 1;
       if (!c.wait(IB_K_FULL + st, (gt / IX_STAGES) & 1)) return;
@@ -160,51 +166,65 @@ __device__ void ix_mma(const IndexerParams& p, const IxCtx& c, uint32_t tbase) {
       mma_commit(c.bar(IB_K_EMPTY + st));
       mma_commit(c.bar(IB_D_FULL + db));
     }
-    mma_commit(c.bar(IB_Q_FREE));
+    mma_commit(c.bar(IB_Q_FREE + qb));
     ++n;
   }
 }
 
-__device__ void ix_epilogue(const IndexerParams& p, const IxCtx& c, uint32_t tbase, int i) {
+// Epilogue warpgroup `grp` (0: warps 0-3, 1: warps 4-7; thread i = TMEM lane = cached token)
+// takes the group's query tokens q with q % 2 == grp.  Each warp stages the item's head
+// weights in its own shared-memory slice (no barrier beyond the warp) and reads them four at a
+// time; a token's 64 accumulator columns are loaded before one wait.
+__device__ void ix_epilogue(const IndexerParams& p, const IxCtx& c, uint32_t tbase, int i,
+                            int grp, float* wsm) {
   const uint32_t lane_base = static_cast<uint32_t>((i >> 5) * 32) << 16;
+  const int lane = i & 31;
   uint32_t gt = 0;
   for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
     const IxItem it = item_of(p, item);
     if (it.tile0 >= it.tile1) continue;
     const int32_t* row = p.table + static_cast<size_t>(it.req) * p.max_pages;
-    int lens[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) lens[q] = q < it.gs ? p.valid_len[it.t0 + q] : 0;
+    __syncwarp();
+    for (int k = lane; k < it.gs * 64; k += 32) wsm[k] = __ldg(p.w + static_cast<size_t>(it.t0) * 64 + k);
+    __syncwarp();
+    // the key scale of this thread's token, one tile ahead (the page-table entry and then the
+    // scale are two dependent loads; they overlap the wait for the tile's products)
+    auto scale_of = [&](int tile) -> float {
+      const int s = tile * IX_TILE + i;
+      if (tile >= it.tile1 || s >= it.maxlen) return 0.f;
+      const int page = row[s / 64];
+      if (page < 0 || page >= p.num_pages) return 0.f;  // outside the cache: zero codes, score 0
+      return __ldg(reinterpret_cast<const float*>(p.cache + static_cast<size_t>(page) * IX_PAGE_BYTES +
+                                                  8192) + (s & 63));
+    };
+    float next_scale = scale_of(it.tile0);
     for (int tile = it.tile0; tile < it.tile1; ++tile, ++gt) {
       const uint32_t db = gt & 1;
+      const float scale = next_scale;
+      next_scale = scale_of(tile + 1);
       if (!c.wait_warp(IB_D_FULL + db, (gt >> 1) & 1)) return;
       tc_fence_after();
       const int s = tile * IX_TILE + i;  // this thread's cached token
-      float scale = 0.f;  // a page id outside the cache reads as zero codes: score 0
-      if (s < it.maxlen) {
-        const int page = row[s / 64];
-        if (page >= 0 && page < p.num_pages)
-          scale = __ldg(reinterpret_cast<const float*>(p.cache + static_cast<size_t>(page) * IX_PAGE_BYTES +
-                                                        8192) + (s & 63));
-      }
-      for (int q = 0; q < it.gs; ++q) {
-        const float* wq = p.w + static_cast<size_t>(it.t0 + q) * 64;
-        float acc0 = 0.f, acc1 = 0.f;
+      for (int q = grp; q < it.gs; q += 2) {
+        uint32_t r[64];
 #pragma unroll
-        for (int jc = 0; jc < 4; ++jc) {
-          uint32_t r[16];
-          tmem_ld16(tbase + lane_base + db * 256 + q * 64 + jc * 16, r);
-          tmem_wait_ld();
+        for (int jc = 0; jc < 4; ++jc) tmem_ld16(tbase + lane_base + db * 256 + q * 64 + jc * 16, r + 16 * jc);
+        tmem_wait_ld();
+        const float4* wq = reinterpret_cast<const float4*>(wsm + q * 64);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            acc0 = fmaf(__ldg(wq + jc * 16 + e), fmaxf(__uint_as_float(r[e]), 0.f), acc0);
-            acc1 = fmaf(__ldg(wq + jc * 16 + e + 1), fmaxf(__uint_as_float(r[e + 1]), 0.f), acc1);
-          }
+        for (int e = 0; e < 16; ++e) {
+          const float4 wv = wq[e];
+          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * e]), 0.f), acc[0]);
+          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * e + 1]), 0.f), acc[1]);
+          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * e + 2]), 0.f), acc[2]);
+          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * e + 3]), 0.f), acc[3]);
         }
-        int n = lens[q];
+        int n = p.valid_len[it.t0 + q];
         n = n > p.ld ? p.ld : n;
         n = n > p.max_pages * 64 ? p.max_pages * 64 : n;
-        if (s < n) p.out[static_cast<size_t>(it.t0 + q) * p.ld + s] = (acc0 + acc1) * scale;
+        if (s < n)
+          p.out[static_cast<size_t>(it.t0 + q) * p.ld + s] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
       }
       tc_fence_before();
       mbar_arrive(c.bar(IB_D_EMPTY + db));
@@ -229,14 +249,16 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(c.bar(IB_D_FULL + b), 1);
-      mbar_init(c.bar(IB_D_EMPTY + b), 128);
+      mbar_init(c.bar(IB_D_EMPTY + b), 256);
     }
-    mbar_init(c.bar(IB_Q_FULL), 1);
-    mbar_init(c.bar(IB_Q_FREE), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(c.bar(IB_Q_FULL + b), 1);
+      mbar_init(c.bar(IB_Q_FREE + b), 1);
+    }
     mbar_init(c.bar(IB_DRAIN), 1);
     fence_mbar_init_cluster();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(c.sbase + IX_OFF_MISC, 512);
     tmem_relinquish();
   }
@@ -244,9 +266,10 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + IX_OFF_MISC);
-  if (warp < 4) {
-    ix_epilogue(p, c, tbase, threadIdx.x);
-  } else if (warp == 4) {
+  if (warp < 8) {
+    ix_epilogue(p, c, tbase, threadIdx.x & 127, warp >> 2,
+                reinterpret_cast<float*>(sm + IX_OFF_W) + warp * 256);
+  } else if (warp == 8) {
     if (lane == 0) ix_producer(p, c);
   } else if (lane == 0) {
     ix_mma(p, c, tbase);
@@ -259,7 +282,7 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tbase, 512);
+  if (warp == 9) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
