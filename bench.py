@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 One step = the whole hot path on one batch: split-KV plan (sched_meta), decode pass, combine,
-all through the C ABI, inputs resident in HBM.  L2 is flushed (a 256 MiB write) between
-steps; the flush is outside the step time.  Prints one JSON line (rank 0).
+all through the C ABI, inputs resident in HBM.  L2 is flushed between steps (a 256 MiB
+write, then a 256 MiB read of another buffer that writes the dirty lines back); the flush is
+outside the step time.  Prints one JSON line (rank 0).
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the same
 workload (the reference arm of this project: the pages ship no runnable code).
@@ -26,6 +27,9 @@ import sys
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(ROOT, "sparse_mla_attention_decode_gb300", "csrc")
+FLUSH_NOTE = ("flushed between steps (256 MiB write, then a 256 MiB read of another buffer so "
+              "no dirty line is left; outside the step time)")
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse MLA decode TFLOPS & gathered KV tokens/s, % of roofline (1×GB300)"
@@ -60,10 +64,13 @@ def dist_env():
     return ws, rank, local
 
 
-def traffic_from_profiles(kernel_src: str, workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, or None when the summary
-    is missing, is for another workload, or was taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+def traffic_from_profiles(kernel_src: str, profile: str, alg_bytes=None):
+    """DRAM bytes per launch from a committed ncu summary, or None when the summary is missing
+    or was taken on a different kernel source.  A summary captured on a smaller case than the
+    bench's records its own algorithmic bytes; its traffic is then scaled by the ratio of the
+    algorithmic bytes (the kernel reads each valid input byte once, so traffic grows in
+    proportion)."""
+    path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
     txt = open(path, encoding="utf-8").read()
@@ -72,7 +79,28 @@ def traffic_from_profiles(kernel_src: str, workload: str):
     if not m_src or not m_b:
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return float(m_b.group(1)) if m_src.group(1) == sha else None
+    if m_src.group(1) != sha:
+        return None
+    traffic = float(m_b.group(1))
+    m_a = re.search(r"alg_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if alg_bytes is not None and m_a:
+        traffic *= float(alg_bytes) / float(m_a.group(1))
+    return traffic
+
+
+class L2Flush:
+    """Leaves L2 holding none of the next step's inputs and no dirty line: a 256 MiB write
+    (larger than L2), then a 256 MiB read of a second buffer, which writes the dirty lines back
+    before the timed step starts instead of during it."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self, k: int = 1):
+        self.w.fill_(k & 0xFF)
+        self.r.max()
 
 
 class ClockSampler:
@@ -254,6 +282,8 @@ def run_topk(args):
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     peak = float(peaks["hbm_gbs"])
     achieved = alg / t / 1e9
+    traffic = traffic_from_profiles(os.path.join(CSRC, "topk.cu"),
+                                    "topk_kernel_prefill_1024x65536_k2048.md", alg)
     print(json.dumps({
         "metric": "exact top-k + page-table emit, index-score bytes/s", "impl": "gb300",
         "value": achieved, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
@@ -262,9 +292,69 @@ def run_topk(args):
         "config": {"workload": f"topk_prefill_{n_tok}x{ld}_k{k}", "rows": n_tok, "ld": ld,
                    "topk": k, "causal_base": 61440, "l2": "inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": "measured copy bandwidth", "alg_bytes_per_launch": alg},
         "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+
+
+def run_indexer(args):
+    """The lightning-indexer scores on the decode workload's shape: 64 requests, one query token
+    each, over 32768 cached tokens (512 indexer pages of 8448 bytes) per request.  HBM-bound: the
+    algorithmic bytes are the key pages read once per request (132 bytes a token), the fp32
+    scores written and the e4m3 Q and fp32 weights read.  L2 is flushed between steps (the
+    277 MB of pages are larger than L2 too)."""
+    import torch
+
+    import sparse_mla_attention_decode_gb300 as smla
+    import workloads
+
+    dev = torch.device("cuda:0")
+    b, ctx = 64, 32768
+    pages = ctx // 64
+    cache = workloads.indexer_cache(b * pages, seed=1, device=dev)
+    q8, w = workloads.indexer_queries(b, seed=2, device=dev)
+    table = torch.randperm(b * pages, generator=torch.Generator().manual_seed(3))
+    table = table.to(torch.int32).view(b, pages).to(dev)
+    lens = torch.full((b,), ctx, dtype=torch.int32, device=dev)
+    out = torch.empty(b, ctx, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush()
+        smla.indexer_scores(q8, w, cache, table, lens, 1, ctx, out=out)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ts = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        smla.indexer_scores(q8, w, cache, table, lens, 1, ctx, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    clocks = sampler.stop()
+    t = sum(ts) / len(ts)
+    alg = b * ctx * 132 + b * ctx * 4 + b * (64 * 128 + 64 * 4)
+    flops = 2.0 * 64 * 128 * b * ctx
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    peak = float(peaks["hbm_gbs"])
+    achieved = alg / t / 1e9
+    traffic = traffic_from_profiles(os.path.join(CSRC, "indexer.cu"),
+                                    f"indexer_kernel_decode_b{b}_ctx{ctx}.md", alg)
+    print(json.dumps({
+        "metric": "lightning-indexer scores (e4m3 tensor-core MMA + ReLU + weighted head sum), "
+                  "bytes/s", "impl": "gb300", "value": achieved, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": f"indexer_decode_b{b}_ctx{ctx}", "requests": b, "ctx": ctx,
+                   "heads": 64, "dim": 128, "l2": FLUSH_NOTE},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": "measured copy bandwidth", "alg_bytes_per_launch": alg},
+        "tflops": flops / t / 1e12, "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
 
 def main():
@@ -278,7 +368,7 @@ def main():
                     help="seconds of oracle time for the cpu_baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", default="decode", choices=["decode", "topk"],
+    ap.add_argument("--kernel", default="decode", choices=["decode", "topk", "indexer"],
                     help="decode: the attention path (the default line); topk: the top-k "
                          "selection with the page-table emit, on its own line")
     ap.add_argument("--topk-rows", type=int, default=4096)
@@ -288,6 +378,8 @@ def main():
         return run_reference(args)
     if args.kernel == "topk":
         return run_topk(args)
+    if args.kernel == "indexer":
+        return run_indexer(args)
 
     import numpy as np
     import torch
@@ -310,7 +402,7 @@ def main():
                               num_sms=num_sms)
     out = torch.empty(spec.b, spec.s_q, spec.h_q, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(spec.b, spec.h_q, spec.s_q, dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     st = stream.cuda_stream
     d = op.dims
@@ -341,7 +433,7 @@ def main():
             ev[1].record(stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush()
         step()
     torch.cuda.synchronize(dev)
     if op.device_status() != 0:
@@ -357,13 +449,13 @@ def main():
     time.sleep(0.3)
     t0 = time.perf_counter()
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        flush(k)
         step(evs[k])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
     # the decode kernel alone (for the roofline): events on the launching stream around it
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        flush(k)
         sched()
         dec_evs[k][0].record(stream)
         decode()
@@ -391,8 +483,8 @@ def main():
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / t_dec / 1e12
-    traffic = traffic_from_profiles(
-        os.path.join(ROOT, "sparse_mla_attention_decode_gb300", "csrc", "decode_fwd.cu"), spec.name)
+    traffic = traffic_from_profiles(os.path.join(CSRC, "decode_fwd.cu"),
+                                    f"decode_kernel_{spec.name}.md")
 
     # ---- end to end through the public API with host buffers (KV cache resident)
     q_h = wl.q.cpu().pin_memory()
@@ -414,7 +506,7 @@ def main():
     torch.cuda.synchronize(dev)
     e_times = []
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        flush(k)
         torch.cuda.synchronize(dev)
         t1 = time.perf_counter()
         e2e_step()
@@ -444,7 +536,7 @@ def main():
             "config": {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
                        "topk": spec.topk, "ctx": spec.ctx, "num_blocks": int(wl.kv.shape[0]),
                        "valid_slots": nvalid, "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
-                       "l2": "flushed between steps (256 MiB write, outside the step time)"},
+                       "l2": FLUSH_NOTE},
             "gathered_tokens_per_s": ws * nvalid / t_step,
             "tflops_all_slots": ws * flops_all / t_step / 1e12,
             "kernel_ms": {"decode": statistics.mean(dec_ms),
