@@ -122,7 +122,7 @@ bool smla::encode_rows_map(CUtensorMap* map, const void* base, bool fp32, int64_
 }
 
 bool smla::encode_bytes_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides, const uint32_t* box) {
+                            const uint64_t* strides, const uint32_t* box, bool swizzle128) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint64_t d[3], st[2];
@@ -134,7 +134,8 @@ bool smla::encode_bytes_map(CUtensorMap* map, const void* base, int rank, const 
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank),
              const_cast<void*>(base), d, st, bx, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -367,8 +368,16 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* d, int num_sms, c
   const uint64_t qd[2] = {128, static_cast<uint64_t>(d->n_tok) * 64};
   const uint64_t qs[1] = {128};
   const uint32_t qb[2] = {128, static_cast<uint32_t>(64 * G)};
-  const void* kbase = d->num_pages > 0 ? k_cache : q8;  // any valid address when there is no page
-  if (!encode_bytes_map(&L.k_map, kbase, 3, kd, ks, kb) || !encode_bytes_map(&L.q_map, q8, 2, qd, qs, qb))
+  // the key scales of a page: 256 bytes at offset 8192, one row per page
+  const uint64_t sd[2] = {256, kd[2]};
+  const uint64_t ss[1] = {8448};
+  const uint32_t sb[2] = {256, 1};
+  // with no page at all both maps point at q8 (its first 8192 bytes are readable) and the
+  // kernel takes every key scale as 0
+  const void* kbase = d->num_pages > 0 ? k_cache : q8;
+  const void* sbase = d->num_pages > 0 ? static_cast<const void*>(static_cast<const uint8_t*>(k_cache) + 8192) : q8;
+  if (!encode_bytes_map(&L.k_map, kbase, 3, kd, ks, kb) || !encode_bytes_map(&L.q_map, q8, 2, qd, qs, qb) ||
+      !encode_bytes_map(&L.s_map, sbase, 2, sd, ss, sb, false))
     return SMLA_ERR_CUDA;
   L.w = weights;
   L.table = block_table;

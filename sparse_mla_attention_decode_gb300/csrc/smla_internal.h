@@ -103,7 +103,7 @@ cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream)
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 // Indexer scores (csrc/indexer.cu): the tensor maps are encoded by the host API.
 struct IndexerLaunch {
-  CUtensorMap k_map, q_map;
+  CUtensorMap k_map, q_map, s_map;
   const float* w;
   const int32_t* table;
   const int32_t* valid_len;
@@ -114,9 +114,10 @@ struct IndexerLaunch {
   int64_t num_pages;
 };
 cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream);
-// Encodes a byte tensor map with a 128-byte swizzle: dims / strides (bytes) / box, 2 or 3 dims.
+// Encodes a byte tensor map, with a 128-byte swizzle unless swizzle128 is false: dims /
+// strides (bytes) / box, 2 or 3 dims.
 bool encode_bytes_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides, const uint32_t* box);
+                      const uint64_t* strides, const uint32_t* box, bool swizzle128 = true);
 cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
                         const int32_t* table, int32_t* out, uint32_t* status, int n_tok, int s_q,
                         int k, int ld, int max_pages, cudaStream_t stream);
