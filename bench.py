@@ -357,6 +357,69 @@ def run_indexer(args):
         "tflops": flops / t / 1e12, "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
 
+def run_select(args):
+    """The two selection steps chained (indexer scores -> exact top-k with the page-table emit,
+    the scores only in an L2-sized scratch) on the decode workload's shape: 64 requests, one
+    query token each, 32768 cached tokens, k = 2048.  HBM-bound; the algorithmic bytes are the
+    indexer pages read once, Q and weights, and the ids written (the scores never reach HBM by
+    design, so they are not counted).  L2 is flushed between steps."""
+    import torch
+
+    import sparse_mla_attention_decode_gb300 as smla
+    import workloads
+
+    dev = torch.device("cuda:0")
+    b, ctx, k = 64, 32768, 2048
+    pages = ctx // 64
+    cache = workloads.indexer_cache(b * pages, seed=1, device=dev)
+    q8, w = workloads.indexer_queries(b, seed=2, device=dev)
+    table = torch.randperm(b * pages, generator=torch.Generator().manual_seed(3))
+    table = table.to(torch.int32).view(b, pages).to(dev)
+    lens = torch.full((b,), ctx, dtype=torch.int32, device=dev)
+    out = torch.empty(b, k, dtype=torch.int32, device=dev)
+    d = smla.smla_indexer_dims(b, 1, 64, 128, pages, ctx, b * pages)
+    scratch = torch.empty(smla.sparse_mla_indexer_topk_scratch_size(d), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        smla.indexer_topk(q8, w, cache, table, lens, 1, ctx, k, out=out, scratch=scratch)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ts = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    clocks = sampler.stop()
+    t = sum(ts) / len(ts)
+    alg = b * pages * 8448 + b * (64 * 128 + 64 * 4) + b * k * 4
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    peak = float(peaks["hbm_gbs"])
+    achieved = alg / t / 1e9
+    print(json.dumps({
+        "metric": "indexer scores + exact top-k chained (scores kept in L2), bytes/s",
+        "impl": "gb300", "value": achieved, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "dtype": "e4m3 x e4m3 -> f32 scores", "data": "synthetic",
+        "config": {"workload": f"select_decode_b{b}_ctx{ctx}_k{k}", "requests": b, "ctx": ctx,
+                   "topk": k, "scratch_bytes": scratch.numel(), "l2": FLUSH_NOTE},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": "measured copy bandwidth", "alg_bytes_per_launch": alg},
+        "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,9 +431,10 @@ def main():
                     help="seconds of oracle time for the cpu_baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", default="decode", choices=["decode", "topk", "indexer"],
+    ap.add_argument("--kernel", default="decode", choices=["decode", "topk", "indexer", "select"],
                     help="decode: the attention path (the default line); topk: the top-k "
-                         "selection with the page-table emit, on its own line")
+                         "selection with the page-table emit; indexer: the indexer scores; "
+                         "select: the two chained; each on its own line")
     ap.add_argument("--topk-rows", type=int, default=4096)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -380,6 +444,8 @@ def main():
         return run_topk(args)
     if args.kernel == "indexer":
         return run_indexer(args)
+    if args.kernel == "select":
+        return run_select(args)
 
     import numpy as np
     import torch

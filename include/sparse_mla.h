@@ -344,6 +344,40 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* dims, int num_sms
                                       const int32_t* block_table, const int32_t* valid_len,
                                       float* scores, uint32_t* status, void* stream);
 
+/*
+ * sparse_mla_indexer_topk -- the two selection steps chained, without the [n_tok][ld] score
+ * matrix ("FlashMLA 与 DSA", sections 4.1, 5.3 and 5.5; "sparse-attention co-design",
+ * section 5, steps one to five: the indexer scores feed the top-k and only the selected ids
+ * are kept).  For each run of query tokens whose scores fit `scratch`, the indexer scores
+ * (as sparse_mla_indexer_scores) go into scratch and the exact top-k with the page-table emit
+ * (as sparse_mla_topk_page_table on fp32 scores) reads them back, so the scores of at most
+ * scratch_bytes / (L * 4) tokens exist at a time; with the scratch the size helper returns
+ * (SMLA_SELECT_SCRATCH_BUDGET bytes or less) they stay in L2 between the two steps.
+ * Positions considered for token t: s < min(valid_len[t], L), L = min(dims->ld,
+ * dims->max_pages * 64).
+ *   dims             as for sparse_mla_indexer_scores; dims->ld (a multiple of 4) bounds the
+ *                    positions and no score matrix of that stride is needed
+ *   topk             output slots per token (>= 1)
+ *   q8, weights, k_cache, block_table, valid_len   as for sparse_mla_indexer_scores
+ *   scratch          device buffer, 16-byte aligned, at least L * 4 bytes (one token's
+ *                    scores); its contents on return are unspecified
+ *   out_indices      device int32 [n_tok][topk] (written), as for sparse_mla_topk_page_table
+ *   status           optional device uint32 word (SMLA_DEV_TIMEOUT, SMLA_DEV_TOPK_TABLE)
+ * Launches two kernels per run of tokens, all on stream, asynchronously.  Errors:
+ * SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_ALIGNMENT (also ld not a multiple of
+ * 4), SMLA_ERR_WORKSPACE (scratch below one token's scores), SMLA_ERR_CUDA.
+ *
+ * sparse_mla_indexer_topk_scratch_size -- host only: the scratch bytes for dims: the scores
+ * of min(n_tok, max(1, SMLA_SELECT_SCRATCH_BUDGET / (L * 4))) tokens.
+ */
+#define SMLA_SELECT_SCRATCH_BUDGET (48u << 20)
+smla_status sparse_mla_indexer_topk_scratch_size(const smla_indexer_dims* dims, size_t* bytes);
+smla_status sparse_mla_indexer_topk(const smla_indexer_dims* dims, int32_t topk, int num_sms,
+                                    const void* q8, const float* weights, const void* k_cache,
+                                    const int32_t* block_table, const int32_t* valid_len,
+                                    void* scratch, size_t scratch_bytes, int32_t* out_indices,
+                                    uint32_t* status, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* sparse_mla_status_string(smla_status status);
 

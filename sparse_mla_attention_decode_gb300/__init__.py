@@ -24,7 +24,8 @@ __all__ = [
     "sparse_mla_plan_has_splits", "smla_topk_dims", "sparse_mla_topk_page_table",
     "topk_page_table", "SMLA_SCORES_BF16", "SMLA_SCORES_FP32",
     "smla_indexer_dims", "sparse_mla_indexer_scores", "indexer_scores",
-    "SparseMLADecode", "dims_for",
+    "sparse_mla_indexer_topk_scratch_size", "sparse_mla_indexer_topk", "indexer_topk",
+    "SELECT_SCRATCH_BUDGET", "SparseMLADecode", "dims_for",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +42,10 @@ EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_de
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
             "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
             "sparse_mla_combine_ex", "sparse_mla_plan_has_splits", "sparse_mla_topk_page_table",
-            "sparse_mla_indexer_scores"]
+            "sparse_mla_indexer_scores", "sparse_mla_indexer_topk_scratch_size",
+            "sparse_mla_indexer_topk"]
+# Scratch budget of the chained selection (SMLA_SELECT_SCRATCH_BUDGET): scores kept in L2.
+SELECT_SCRATCH_BUDGET = 48 << 20
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -116,6 +120,9 @@ def lib():
             L.sparse_mla_topk_page_table.argtypes = [P(smla_topk_dims), vp, vp, vp, vp, vp, vp]
             L.sparse_mla_indexer_scores.argtypes = [P(smla_indexer_dims), ctypes.c_int, vp, vp, vp,
                                                     vp, vp, vp, vp, vp]
+            L.sparse_mla_indexer_topk_scratch_size.argtypes = [P(smla_indexer_dims), P(sz)]
+            L.sparse_mla_indexer_topk.argtypes = [P(smla_indexer_dims), ctypes.c_int32, ctypes.c_int,
+                                                  vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
             L.sparse_mla_status_string.argtypes = [ctypes.c_int]
             L.sparse_mla_status_string.restype = ctypes.c_char_p
             L.sparse_mla_read_device_status.argtypes = [P(smla_dims), ctypes.c_int, vp,
@@ -278,6 +285,49 @@ def indexer_scores(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: i
     sparse_mla_indexer_scores(d, num_sms, q8.data_ptr(), weights.data_ptr(), k_cache.data_ptr(),
                               block_table.data_ptr(), valid_len.data_ptr(), out.data_ptr(),
                               status.data_ptr() if status is not None else 0, st)
+    return out
+
+
+def sparse_mla_indexer_topk_scratch_size(dims: smla_indexer_dims) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().sparse_mla_indexer_topk_scratch_size(ctypes.byref(dims), ctypes.byref(n)),
+           "sparse_mla_indexer_topk_scratch_size")
+    return n.value
+
+
+def sparse_mla_indexer_topk(dims: smla_indexer_dims, topk: int, num_sms: int, q8: int,
+                            weights: int, k_cache: int, block_table: int, valid_len: int,
+                            scratch: int, scratch_bytes: int, out_indices: int, status: int = 0,
+                            stream: int = 0) -> None:
+    _check(lib().sparse_mla_indexer_topk(ctypes.byref(dims), int(topk), int(num_sms), q8, weights,
+                                         k_cache, block_table, valid_len, scratch,
+                                         int(scratch_bytes), out_indices, status or None, stream),
+           "sparse_mla_indexer_topk")
+
+
+def indexer_topk(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: int, k: int,
+                 out=None, scratch=None, status=None, num_sms: int = 0, stream=None):
+    """The indexer scores and their exact top-k chained (int32 ids [n_tok, k], -1 padding)
+    without the [n_tok, ld] score matrix: the scores of one run of tokens at a time live in
+    ``scratch`` (uint8 device tensor; by default the size the library asks for)."""
+    import torch
+    for name, t, dt in (("q8", q8, torch.uint8), ("weights", weights, torch.float32),
+                        ("k_cache", k_cache, torch.uint8), ("block_table", block_table, torch.int32),
+                        ("valid_len", valid_len, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor")
+    n_tok = q8.shape[0]
+    d = smla_indexer_dims(n_tok, s_q, 64, 128, block_table.shape[1], ld, k_cache.shape[0])
+    if scratch is None:
+        scratch = torch.empty(sparse_mla_indexer_topk_scratch_size(d), dtype=torch.uint8,
+                              device=q8.device)
+    if out is None:
+        out = torch.empty(n_tok, k, dtype=torch.int32, device=q8.device)
+    st = (stream if stream is not None else torch.cuda.current_stream(q8.device)).cuda_stream
+    sparse_mla_indexer_topk(d, k, num_sms, q8.data_ptr(), weights.data_ptr(), k_cache.data_ptr(),
+                            block_table.data_ptr(), valid_len.data_ptr(), scratch.data_ptr(),
+                            scratch.numel(), out.data_ptr(),
+                            status.data_ptr() if status is not None else 0, st)
     return out
 
 

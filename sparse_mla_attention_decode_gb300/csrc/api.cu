@@ -394,6 +394,78 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* d, int num_sms, c
   return cuda_status(launch_indexer(L, static_cast<cudaStream_t>(stream)));
 }
 
+// Positions the chained selection considers: min(ld, max_pages * 64), or -1 if dims is bad.
+static int64_t select_len(const smla_indexer_dims* d) {
+  if (!d || d->n_tok < 0 || d->s_q < 1 || d->ld < 0 || d->max_pages < 0) return -1;
+  const int64_t cap = static_cast<int64_t>(d->max_pages) * kPage;
+  return d->ld < cap ? d->ld : cap;
+}
+
+smla_status sparse_mla_indexer_topk_scratch_size(const smla_indexer_dims* d, size_t* bytes) {
+  const int64_t L = select_len(d);
+  if (L < 0 || !bytes) return SMLA_ERR_INVALID_ARG;
+  const int64_t row = L * 4;
+  int64_t rows = row > 0 ? static_cast<int64_t>(SMLA_SELECT_SCRATCH_BUDGET) / row : d->n_tok;
+  if (rows < 1) rows = 1;
+  if (rows > d->n_tok) rows = d->n_tok;
+  *bytes = static_cast<size_t>(rows * (row > 0 ? row : 16));
+  return SMLA_OK;
+}
+
+smla_status sparse_mla_indexer_topk(const smla_indexer_dims* d, int32_t topk, int num_sms,
+                                    const void* q8, const float* weights, const void* k_cache,
+                                    const int32_t* block_table, const int32_t* valid_len,
+                                    void* scratch, size_t scratch_bytes, int32_t* out_indices,
+                                    uint32_t* status, void* stream) {
+  const int64_t L = select_len(d);
+  if (L < 0 || topk < 1) return SMLA_ERR_INVALID_ARG;
+  if (d->heads != 64 || d->dim != 128) return SMLA_ERR_UNSUPPORTED;
+  if (d->n_tok % d->s_q != 0) return SMLA_ERR_INVALID_ARG;
+  if (d->n_tok == 0) return SMLA_OK;
+  if (!scratch || !out_indices || !q8 || !weights || !block_table || !valid_len) return SMLA_ERR_INVALID_ARG;
+  if (d->ld % 4 != 0 || !aligned(scratch, 16)) return SMLA_ERR_ALIGNMENT;
+  const int64_t row = L * 4;
+  if (row > 0 && scratch_bytes < static_cast<size_t>(row)) return SMLA_ERR_WORKSPACE;
+  const int64_t R = row > 0 ? static_cast<int64_t>(scratch_bytes / static_cast<size_t>(row)) : d->n_tok;
+  const int n_req = d->n_tok / d->s_q;
+  const uint8_t* q = static_cast<const uint8_t*>(q8);
+  for (int64_t t = 0; t < d->n_tok;) {
+    const int64_t r = t / d->s_q;
+    int64_t n, sub_sq;
+    if (d->s_q <= R) {  // whole requests
+      int64_t reqs = R / d->s_q;
+      if (reqs > n_req - r) reqs = n_req - r;
+      n = reqs * d->s_q;
+      sub_sq = d->s_q;
+    } else {  // a run of one request's tokens, as a request of its own
+      n = (r + 1) * d->s_q - t;
+      if (n > R) n = R;
+      sub_sq = n;
+    }
+    smla_indexer_dims ix = *d;
+    ix.n_tok = static_cast<int32_t>(n);
+    ix.s_q = static_cast<int32_t>(sub_sq);
+    ix.ld = static_cast<int32_t>(L);
+    const int32_t* table = block_table + r * d->max_pages;
+    smla_status st = sparse_mla_indexer_scores(&ix, num_sms, q + t * 64 * 128, weights + t * 64,
+                                               k_cache, table, valid_len + t,
+                                               static_cast<float*>(scratch), status, stream);
+    if (st != SMLA_OK) return st;
+    smla_topk_dims tk;
+    tk.n_tok = static_cast<int32_t>(n);
+    tk.s_q = static_cast<int32_t>(sub_sq);
+    tk.topk = topk;
+    tk.ld = static_cast<int32_t>(L);
+    tk.max_pages = d->max_pages;
+    tk.dtype = SMLA_SCORES_FP32;
+    st = sparse_mla_topk_page_table(&tk, scratch, valid_len + t, table, out_indices + t * topk,
+                                    status, stream);
+    if (st != SMLA_OK) return st;
+    t += n;
+  }
+  return SMLA_OK;
+}
+
 smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* has_splits) {
   smla_status st = check_dims(dims);
   if (st != SMLA_OK) return st;

@@ -202,3 +202,33 @@ def test_indexer_argument_checks(L):
     assert call(smla.smla_indexer_dims(5, 2, 64, 128, 8, 512, 16)) == 1   # n_tok % s_q
     assert call(smla.smla_indexer_dims(4, 1, 64, 128, 8, 512, 16), fake + 4) == 3  # q8 alignment
     assert call(smla.smla_indexer_dims(0, 1, 64, 128, 8, 512, 16)) == 0   # nothing to do
+
+
+def test_indexer_topk_argument_checks(L):
+    fake = 0x10000
+
+    def call(d, topk=16, scratch=fake, nbytes=1 << 20):
+        return L.sparse_mla_indexer_topk(ctypes.byref(d), topk, 152, fake, fake, fake, fake, fake,
+                                         scratch, nbytes, fake, None, None)
+    ok = smla.smla_indexer_dims(4, 2, 64, 128, 8, 512, 16)
+    assert call(ok, topk=0) == 1                                             # topk
+    assert call(smla.smla_indexer_dims(4, 1, 32, 128, 8, 512, 16)) == 2       # heads
+    assert call(smla.smla_indexer_dims(5, 2, 64, 128, 8, 512, 16)) == 1       # n_tok % s_q
+    assert call(ok, scratch=None) == 1                                        # no scratch
+    assert call(smla.smla_indexer_dims(4, 2, 64, 128, 8, 510, 16)) == 3       # ld % 4
+    assert call(ok, scratch=fake + 8) == 3                                    # scratch alignment
+    assert call(ok, nbytes=512 * 4 - 16) == 4                                 # below one token
+    assert call(smla.smla_indexer_dims(0, 1, 64, 128, 8, 512, 16)) == 0       # nothing to do
+
+
+def test_indexer_topk_scratch_size(L):
+    def size(d):
+        n = ctypes.c_size_t()
+        assert L.sparse_mla_indexer_topk_scratch_size(ctypes.byref(d), ctypes.byref(n)) == 0
+        return n.value
+    # positions = min(ld, max_pages * 64); rows = min(n_tok, budget // (positions * 4))
+    assert size(smla.smla_indexer_dims(64, 1, 64, 128, 512, 32768, 1)) == 64 * 32768 * 4
+    assert size(smla.smla_indexer_dims(64, 1, 64, 128, 100, 32768, 1)) == 64 * 6400 * 4
+    big = smla.smla_indexer_dims(4096, 4096, 64, 128, 1024, 65536, 1)
+    assert size(big) == (smla.SELECT_SCRATCH_BUDGET // (65536 * 4)) * 65536 * 4
+    assert size(smla.smla_indexer_dims(3, 1, 64, 128, 1 << 20, 1 << 26, 1)) == (1 << 26) * 4

@@ -125,9 +125,10 @@ def test_combine_kernel_vs_oracle(dev):
     st = torch.cuda.current_stream().cuda_stream
     smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
     torch.cuda.synchronize()
-    meta, pre = op.plan()
-    pre = pre.tolist()
     parts = max(op.num_sms // s_q // 2, 1)
+    # the oracle planner's split layout (the GPU plan must equal it)
+    _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
+    assert op.plan()[1].tolist() == pre
     max_splits = b + parts
     g = torch.Generator(device="cpu").manual_seed(4)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)

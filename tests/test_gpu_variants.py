@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import sched as osched
 import workloads
 from tests import gpu_util as gu
 
@@ -77,9 +78,10 @@ def test_combine_kernel_with_sink(dev):
     st = torch.cuda.current_stream().cuda_stream
     smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
     torch.cuda.synchronize()
-    _, pre = op.plan()
-    pre = pre.tolist()
     parts = max(op.num_sms // s_q // 2, 1)
+    # the oracle planner's split layout (the GPU plan must equal it)
+    _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
+    assert op.plan()[1].tolist() == pre
     max_splits = b + parts
     g = torch.Generator(device="cpu").manual_seed(14)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)
@@ -177,9 +179,10 @@ def test_combine_kernel_bf16_partials(dev):
     st = torch.cuda.current_stream().cuda_stream
     smla.sparse_mla_sched_meta(op.dims, op.num_sms, op.sched.data_ptr(), op.sched_bytes, st)
     torch.cuda.synchronize()
-    _, pre = op.plan()
-    pre = pre.tolist()
     parts = max(op.num_sms // s_q // 2, 1)
+    # the oracle planner's split layout (the GPU plan must equal it)
+    _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
+    assert op.plan()[1].tolist() == pre
     max_splits = b + parts
     g = torch.Generator(device="cpu").manual_seed(15)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g).to(torch.bfloat16)
