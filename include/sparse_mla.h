@@ -338,6 +338,10 @@ typedef struct {
   int32_t max_pages;
   int32_t ld;
   int64_t num_pages;
+  /* 0 normally.  Nonzero: the kernel's MMA issuer waits on a barrier nothing arrives at, so
+   * that every bounded wait runs out (a test of the failure path: SMLA_DEV_TIMEOUT in status,
+   * no score written, the context usable afterwards). */
+  int32_t test_stall;
 } smla_indexer_dims;
 smla_status sparse_mla_indexer_scores(const smla_indexer_dims* dims, int num_sms, const void* q8,
                                       const float* weights, const void* k_cache,

@@ -82,7 +82,7 @@ class smla_topk_dims(ctypes.Structure):
 class smla_indexer_dims(ctypes.Structure):
     _fields_ = [("n_tok", ctypes.c_int32), ("s_q", ctypes.c_int32), ("heads", ctypes.c_int32),
                 ("dim", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("ld", ctypes.c_int32),
-                ("num_pages", ctypes.c_int64)]
+                ("num_pages", ctypes.c_int64), ("test_stall", ctypes.c_int32)]
 
 
 def library_path() -> str:

@@ -391,6 +391,7 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* d, int num_sms, c
   L.ld = d->ld;
   L.num_sms = num_sms;
   L.num_pages = d->num_pages;
+  L.test_stall = d->test_stall;
   return cuda_status(launch_indexer(L, static_cast<cudaStream_t>(stream)));
 }
 

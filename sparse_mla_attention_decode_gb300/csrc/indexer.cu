@@ -44,6 +44,7 @@ enum IxBar {
   IB_Q_FULL = IB_D_EMPTY + 8,               // [2] expect-tx + Q's bytes
   IB_Q_FREE = IB_Q_FULL + 2,                // [2] commit after an item's last MMAs
   IB_DRAIN = IB_Q_FREE + 2,
+  IB_NEVER,                                 // nothing arrives (the failure-path test)
   IB_COUNT
 };
 // Shared memory (base 1024-aligned): barriers, [8 warps][256] head weights (read as float4),
@@ -75,6 +76,7 @@ struct IndexerParams {
   int nshift;  // 1 << nshift TMEM accumulators of 512 >> nshift columns
   int stages;  // key-tile stages
   uint32_t off_sc, off_q, q_bytes;  // shared-memory offsets of the scales and Q buffers
+  int test_stall;                   // the MMA issuer waits on IB_NEVER (bounded) and leaves
   int64_t num_pages;
 };
 
@@ -274,6 +276,10 @@ __device__ void ix_producer(const IndexerParams& p, const IxCtx& c, int lane) {
 }
 
 __device__ void ix_mma(const IndexerParams& p, const IxCtx& c, uint32_t tbase) {
+  if (p.test_stall) {  // the failure-path test: a wait that runs out, before any MMA
+    c.wait(IB_NEVER, 0);
+    return;
+  }
   const uint32_t idesc = umma_idesc_f16(128, 64 * p.G, 0);  // e4m3 x e4m3 -> f32, K-major
   const uint32_t nbuf = 1u << p.nshift, colw = 512u >> p.nshift;
   uint32_t gt = 0, n = 0, st = 0, ph = 0;  // n: Q loads consumed
@@ -440,6 +446,7 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
       mbar_init(c.bar(IB_Q_FREE + b), 1);
     }
     mbar_init(c.bar(IB_DRAIN), 1);
+    mbar_init(c.bar(IB_NEVER), 1);
     fence_mbar_init_cluster();
   }
   if (warp == 9) {
@@ -488,6 +495,7 @@ cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream) {
   p.max_pages = L.max_pages;
   p.ld = L.ld;
   p.num_pages = L.num_pages;
+  p.test_stall = L.test_stall;
   p.G = L.s_q < 4 ? L.s_q : 4;
   p.groups_per_req = (L.s_q + p.G - 1) / p.G;
   p.n_groups = (L.n_tok / L.s_q) * p.groups_per_req;

@@ -112,6 +112,7 @@ struct IndexerLaunch {
   uint32_t* status;
   int n_tok, s_q, max_pages, ld, num_sms;
   int64_t num_pages;
+  int test_stall;
 };
 cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream);
 // Encodes a byte tensor map, with a 128-byte swizzle unless swizzle128 is false: dims /

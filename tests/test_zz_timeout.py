@@ -56,3 +56,42 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(cuda_ok):
     gu.compare(out2.double().cpu().numpy().reshape(-1, 128, 512),
                lse2.double().cpu().numpy().transpose(0, 2, 1).reshape(-1, 128),
                ro.reshape(-1, 128, 512), rl.transpose(0, 2, 1).reshape(-1, 128), "after a timeout")
+
+
+def test_indexer_bounded_wait_runs_out_and_the_context_stays_usable(cuda_ok):
+    # the indexer's MMA issuer waits on a barrier nothing arrives at: the producer (after
+    # waiting for the copies it issued), the epilogue and the issuer all leave their bounded
+    # waits, the status word reports SMLA_DEV_TIMEOUT, no score is written, and the next call
+    # on the same context is correct and clean
+    from oracle import indexer as oix
+    dev = torch.device("cuda:0")
+    b, pages, ld = 2, 40, 2560
+    cache = workloads.indexer_cache(pages, seed=90, device=dev)
+    q8, w = workloads.indexer_queries(b, seed=91, device=dev)
+    table = torch.arange(pages, dtype=torch.int32, device=dev).view(1, pages).repeat(b, 1).contiguous()
+    lens = torch.tensor([ld, 1000], dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.full((b, ld), 7.0, dtype=torch.float32, device=dev)
+    d = smla.smla_indexer_dims(b, 1, 64, 128, pages, ld, pages)
+    d.test_stall = 1
+    st = torch.cuda.current_stream(dev).cuda_stream
+    t0 = time.perf_counter()
+    smla.sparse_mla_indexer_scores(d, 8, q8.data_ptr(), w.data_ptr(), cache.data_ptr(),
+                                   table.data_ptr(), lens.data_ptr(), out.data_ptr(),
+                                   status.data_ptr(), st)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) & smla.SMLA_DEV_TIMEOUT
+    assert 0.5 < elapsed < 10.0, elapsed
+    assert bool(torch.all(out == 7.0)), "no tile reached the epilogue, so no score is written"
+    status.zero_()
+    got = smla.indexer_scores(q8, w, cache, table, lens, 1, ld, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oix.indexer_scores(q8.cpu().numpy(), w.cpu().double().numpy(), cache.cpu().numpy(),
+                             table.cpu().numpy(), lens.cpu().numpy(), 1, ld)
+    g = got.double().cpu().numpy()
+    for t in range(b):
+        n = int(lens[t])
+        tol = 2e-5 * max(1.0, float(np.abs(ref[t, :n]).max())) + 1e-6
+        assert float(np.abs(g[t, :n] - ref[t, :n]).max()) <= tol
