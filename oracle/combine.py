@@ -8,7 +8,7 @@ Source: "FlashMLA 与 DSA：内核、流水线和正确性边界", section 3.2 (
 L = 0) and step 16 (combine: M = max_j lse2_j, weights 2^(lse2_j - M), weighted mean of
 the normalised partial outputs, final lse in natural log).
 
-Reading: when every split has lse2 = -inf the merged output is 0 and the
+Reading (the pages are silent here): when every split has lse2 = -inf the merged output is 0 and the
 merged lse is +inf, the same convention as an unsplit row with no valid slot.
 """
 

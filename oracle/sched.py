@@ -19,7 +19,7 @@ What it computes, in the pages' terms:
 * ``num_splits`` is the prefix sum over requests of the number of partitions that touch
   each request.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * ``end_block`` is exclusive and ``end_req`` is the last request the partition touches.
 * A partition stops as soon as ``remain - 5 <= 0`` would leave it nothing to take.
