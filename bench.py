@@ -88,6 +88,28 @@ def traffic_from_profiles(kernel_src: str, profile: str, alg_bytes=None):
     return traffic
 
 
+def rotated_index_sets(indices, block_table, num_blocks: int, n_sets: int, shift_pages: int = 128):
+    """n_sets index tensors (int32, host): the given one, then the same slots with every valid
+    position of a sequence moved by j * shift_pages pages (cyclically within the sequence's
+    pages) and mapped back through its page table; masked slots stay -1, so the valid count
+    and the FLOPs are the same."""
+    import torch
+    bt = block_table.long().cpu()
+    b, pages = bt.shape
+    inv = torch.zeros(num_blocks, dtype=torch.int64)  # physical page -> its logical index
+    inv[bt.reshape(-1)] = torch.arange(pages).repeat(b)
+    base = indices.long().cpu()
+    seq = torch.arange(b).view(b, *([1] * (base.dim() - 1))).expand_as(base)
+    ok = base >= 0
+    pos = inv[base.clamp(min=0) // 64] * 64 + base.clamp(min=0) % 64
+    out = [indices.cpu().to(torch.int32).contiguous()]
+    for j in range(1, n_sets):
+        moved = (pos + j * shift_pages * 64) % (pages * 64)
+        phys = bt[seq, moved // 64] * 64 + moved % 64
+        out.append(torch.where(ok, phys, base).to(torch.int32).contiguous())
+    return out
+
+
 class L2Flush:
     """Leaves L2 holding none of the next step's inputs and no dirty line: a 256 MiB write
     (larger than L2), then a 256 MiB read of a second buffer, which writes the dirty lines back
@@ -561,18 +583,8 @@ def main():
     # the rows a step gathers out of L2 from the steps before it (4 x 82 MB of rows > L2).
     q_h = wl.q.cpu().pin_memory()
     n_sets = 4
-    i_sets = [wl.indices.cpu().pin_memory()]
-    bt = wl.block_table.long().cpu()
-    pages = bt.shape[1]
-    inv = torch.zeros(wl.kv.shape[0], dtype=torch.int64)
-    inv[bt.reshape(-1)] = torch.arange(pages).repeat(bt.shape[0])
-    base = wl.indices.long().cpu()
-    seq = torch.arange(spec.b).view(spec.b, 1, 1).expand_as(base)
-    for j in range(1, n_sets):
-        pos = inv[base.clamp(min=0) // 64] * 64 + base.clamp(min=0) % 64
-        pos = (pos + j * 128 * 64) % (pages * 64)
-        phys = bt[seq, pos // 64] * 64 + pos % 64
-        i_sets.append(torch.where(base >= 0, phys, base).to(torch.int32).contiguous().pin_memory())
+    i_sets = [s.pin_memory() for s in rotated_index_sets(wl.indices, wl.block_table,
+                                                         wl.kv.shape[0], n_sets)]
     q_d = [torch.empty_like(wl.q) for _ in range(2)]
     i_d = [torch.empty_like(wl.indices) for _ in range(2)]
     o_d = [torch.empty_like(out) for _ in range(2)]
