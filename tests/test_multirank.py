@@ -26,7 +26,7 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_two_gloo_ranks():
     port = 29500 + (os.getpid() % 1000)
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a multi-threaded process
         out = m.dict()
         mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
         assert out[0] == [2.0, 5.0] and out[1] == [2.0, 5.0]
