@@ -309,7 +309,8 @@ def indexer_topk(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: int
                  out=None, scratch=None, status=None, num_sms: int = 0, stream=None):
     """The indexer scores and their exact top-k chained (int32 ids [n_tok, k], -1 padding)
     without the [n_tok, ld] score matrix: the scores of one run of tokens at a time live in
-    ``scratch`` (uint8 device tensor; by default the size the library asks for)."""
+    ``scratch`` (a contiguous device tensor; by default uint8 of the size the library asks
+    for)."""
     import torch
     for name, t, dt in (("q8", q8, torch.uint8), ("weights", weights, torch.float32),
                         ("k_cache", k_cache, torch.uint8), ("block_table", block_table, torch.int32),
@@ -321,12 +322,14 @@ def indexer_topk(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: int
     if scratch is None:
         scratch = torch.empty(sparse_mla_indexer_topk_scratch_size(d), dtype=torch.uint8,
                               device=q8.device)
+    elif not scratch.is_contiguous():
+        raise ValueError("scratch must be contiguous")
     if out is None:
         out = torch.empty(n_tok, k, dtype=torch.int32, device=q8.device)
     st = (stream if stream is not None else torch.cuda.current_stream(q8.device)).cuda_stream
     sparse_mla_indexer_topk(d, k, num_sms, q8.data_ptr(), weights.data_ptr(), k_cache.data_ptr(),
                             block_table.data_ptr(), valid_len.data_ptr(), scratch.data_ptr(),
-                            scratch.numel(), out.data_ptr(),
+                            scratch.numel() * scratch.element_size(), out.data_ptr(),
                             status.data_ptr() if status is not None else 0, st)
     return out
 
