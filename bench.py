@@ -64,22 +64,34 @@ def dist_env():
     return ws, rank, local
 
 
+def code_sha256(path: str) -> str:
+    """sha256 of a source file's code: // and /* */ comments removed, whitespace collapsed, so
+    that a comment edit does not make a profile of an unchanged kernel stale."""
+    txt = open(path, encoding="utf-8").read()
+    txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+    txt = re.sub(r"//[^\n]*", " ", txt)
+    return hashlib.sha256(" ".join(txt.split()).encode()).hexdigest()
+
+
 def traffic_from_profiles(kernel_src: str, profile: str, alg_bytes=None):
     """DRAM bytes per launch from a committed ncu summary, or None when the summary is missing
-    or was taken on a different kernel source.  A summary captured on a smaller case than the
-    bench's records its own algorithmic bytes; its traffic is then scaled by the ratio of the
-    algorithmic bytes (the kernel reads each valid input byte once, so traffic grows in
-    proportion)."""
+    or was taken on different kernel code (its code_sha256, or else its source_sha256, against
+    the current file).  A summary captured on a smaller case than the bench's records its own
+    algorithmic bytes; its traffic is then scaled by the ratio of the algorithmic bytes (the
+    kernel reads each valid input byte once, so traffic grows in proportion)."""
     path = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(path):
         return None
     txt = open(path, encoding="utf-8").read()
+    m_code = re.search(r"code_sha256:\s*([0-9a-f]{64})", txt)
     m_src = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_src or not m_b:
+    if not m_b or not (m_code or m_src):
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    if m_src.group(1) != sha:
+    if m_code:
+        if m_code.group(1) != code_sha256(kernel_src):
+            return None
+    elif m_src.group(1) != hashlib.sha256(open(kernel_src, "rb").read()).hexdigest():
         return None
     traffic = float(m_b.group(1))
     m_a = re.search(r"alg_bytes_per_launch:\s*([0-9.eE+]+)", txt)

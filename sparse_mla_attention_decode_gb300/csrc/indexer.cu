@@ -12,14 +12,16 @@
 // head weights and the 64-head sum stay inside one thread (no transpose, no cross-thread
 // reduction), and the [tokens x heads] products never leave the SM.
 //
-// Work item = (query group of G <= 4 tokens of one request, chunk of key tiles, sized on the
-// host so that the items spread evenly over the SMs); the CTAs walk the items with a grid
-// stride.  Warps 0-7: epilogue, two warpgroups (thread = TMEM lane = token; the even and the
-// odd query tokens of the group); warp 8: TMA producer (Q once per item into one of two
-// buffers; per key tile the two pages' codes and their key scales, eight stages); warp 9: MMA
-// issuer (TMEM accumulators of 64 G columns: eight at G = 1, four at G = 2, two above).  A
-// stage is released by the epilogue once it has read the tile's key scales (the MMAs are done
-// by then), so no global load sits in the epilogue's loop.  Every wait is bounded (a second),
+// Work item = (query group of G <= 4 tokens of one request, chunk of 16 key tiles); each CTA
+// takes an equal contiguous range of the key tiles of all groups laid end to end, so
+// consecutive items share their group's Q.  Warps 0-7: epilogue, two warpgroups (thread =
+// TMEM lane = token) taking alternate (tile, query token) units; warp 8: TMA producer (Q once
+// per run of items of one group into one of two buffers; per key tile the two pages' codes
+// and their key scales, as many stages as fit beside Q); warp 9: MMA issuer (TMEM
+// accumulators of 64 G columns: eight at G = 1, four at G = 2, two above).  A stage is
+// released by the epilogue once it has read the tile's key scales (the MMAs are done by then),
+// and the page ids, lengths and head weights of the next item load while the current one
+// runs, so no global load sits on a role's critical path.  Every wait is bounded (a second),
 // after which the CTA raises SMLA_DEV_TIMEOUT and its roles leave.
 #include <cstdint>
 

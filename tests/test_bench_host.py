@@ -31,3 +31,24 @@ def test_rotation_is_a_shift_of_logical_positions():
     idx = torch.tensor([[[0, 5, 64, 130, -1, 511]]], dtype=torch.int32)
     s = bench.rotated_index_sets(idx, bt, 8, 2, shift_pages=2)[1]
     assert s.tolist() == [[[128, 133, 192, 258, -1, (511 + 128) % 512]]]
+
+
+def test_code_hash_ignores_comments_and_whitespace_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) {  /* a\\nblock */ return x + 1; }  // tail\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// another header\n\nint f(int x) {\n  return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.code_sha256(str(a)) == bench.code_sha256(str(b))
+    assert bench.code_sha256(str(a)) != bench.code_sha256(str(c))
+
+
+def test_committed_profiles_match_the_current_kernels():
+    # each kernel's ncu summary was taken on the code that is in the tree now
+    import os
+    csrc = os.path.join(bench.ROOT, "sparse_mla_attention_decode_gb300", "csrc")
+    for src, prof in (("decode_fwd.cu", "decode_kernel_c2_b64_h128_k2048_mask5.md"),
+                      ("topk.cu", "topk_kernel_prefill_1024x65536_k2048.md"),
+                      ("indexer.cu", "indexer_kernel_decode_b64_ctx32768.md")):
+        assert bench.traffic_from_profiles(os.path.join(csrc, src), prof) is not None, prof
