@@ -75,3 +75,31 @@ def check_row(got: np.ndarray, scores_row: np.ndarray, valid_len: int, k: int,
     assert np.all(vals[pos] >= thr), "a selected score is below the k-th largest value"
     above = np.nonzero(vals > thr)[0]
     assert np.isin(above, pos).all(), "a score above the k-th largest value was left out"
+
+
+def check_row_within(got: np.ndarray, scores_row: np.ndarray, valid_len: int, k: int,
+                     table_row: np.ndarray, tol: float, page: int = 64) -> None:
+    """``check_row`` for scores known only to within ``tol`` (the selection was made on scores
+    computed in lower precision): the selected ids first, then -1; no duplicate; every
+    selected position valid and scoring at least the k-th largest value minus tol; every
+    position scoring above the k-th largest value plus tol selected.  With tol = 0 this is
+    ``check_row``."""
+    n = max(0, min(int(valid_len), scores_row.shape[0]))
+    m = min(k, n)
+    got = np.asarray(got, dtype=np.int64)
+    assert got.shape == (k,)
+    assert np.all(got[m:] == -1), "entries after the selected ones must be -1"
+    ids = got[:m]
+    assert np.all(ids >= 0), "a selected entry is -1"
+    assert np.unique(ids).size == m, "duplicate ids"
+    inv = {int(pg): j for j, pg in enumerate(np.asarray(table_row, dtype=np.int64))}
+    pos = np.array([inv[int(i) // page] * page + int(i) % page for i in ids], dtype=np.int64)
+    assert np.all(pos < n), "a selected position is outside the valid prefix"
+    if m == 0:
+        return
+    _, thr = topk_positions(scores_row, n, k)
+    vals = np.asarray(scores_row[:n], dtype=np.float64)
+    assert np.all(vals[pos] >= thr - tol), "a selected score is below the k-th largest value"
+    above = np.nonzero(vals > thr + tol)[0]
+    assert np.isin(above, pos).all(), "a score above the k-th largest value was left out"
+

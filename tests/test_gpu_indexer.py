@@ -168,26 +168,6 @@ def test_indexer_topk_chain(dev, case):
         assert set(got[t, :m].tolist()) == set(ridx[t, :m].tolist()), t
 
 
-def _check_selection(got, scores, n, k, table_row, tol):
-    """A correct top-k of the oracle scores within the GPU's score tolerance: the selected
-    ids first, then -1; no duplicate; every position scoring above the k-th largest value plus
-    tol is selected, and none scoring below it minus tol."""
-    m = min(n, k)
-    assert np.all(got[m:] == -1)
-    ids = got[:m].astype(np.int64)
-    assert np.all(ids >= 0) and np.unique(ids).size == m
-    inv = {int(pg): j for j, pg in enumerate(np.asarray(table_row, dtype=np.int64))}
-    pos = np.array([inv[int(i) // 64] * 64 + int(i) % 64 for i in ids], dtype=np.int64)
-    assert np.all(pos < n)
-    if n <= k:
-        return
-    v = scores[:n]
-    thr = np.sort(v)[::-1][k - 1]
-    assert np.all(v[pos] >= thr - tol), "a selected score is below the threshold"
-    above = np.nonzero(v > thr + tol)[0]
-    assert np.isin(above, pos).all(), "a score above the threshold was left out"
-
-
 def test_indexer_topk_chain_decode_shape(dev):
     # the bench's shape (64 requests x 32768 cached tokens, k = 2048), one run in the default
     # scratch; sampled rows against the oracle.  With 32768 positions the gap at the k-th
@@ -208,4 +188,4 @@ def test_indexer_topk_chain_decode_shape(dev):
     for j, t in enumerate(rows):
         n = min(int(lens[t]), ld)
         tol = 2e-5 * max(1.0, float(np.abs(rs[j, :n]).max())) + 1e-6
-        _check_selection(got[t], rs[j], n, k, table[t].numpy(), tol)
+        otk.check_row_within(got[t], rs[j], n, k, table[t].numpy(), tol)

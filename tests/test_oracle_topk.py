@@ -80,3 +80,34 @@ def test_checker_rejects_planted_mistakes():
     b = ids2[0].copy(); b[0] = otk.emit_ids([250], table)[0]
     with pytest.raises(AssertionError):
         otk.check_row(b, scores, 100, k, table)
+
+
+def test_check_row_within_accepts_near_ties_and_rejects_planted_mistakes():
+    rng = np.random.default_rng(11)
+    n, k = 300, 40
+    table = rng.permutation(20)[:5]
+    vals = rng.standard_normal(n)
+    order = np.argsort(-vals)
+    thr = vals[order[k - 1]]
+    tol = 1e-3
+    vals[order[k]] = thr - tol / 2  # the (k+1)-th largest within tol of the k-th
+    good = otk.emit_ids(order[:k], table)
+    otk.check_row_within(np.asarray(good), vals, n, k, table, tol)
+    # swapping the k-th for the near-tie is also a correct answer within tol
+    swapped = otk.emit_ids(np.r_[order[: k - 1], order[k]], table)
+    otk.check_row_within(np.asarray(swapped), vals, n, k, table, tol)
+    with pytest.raises(AssertionError):  # ... but not at tol = 0
+        otk.check_row_within(np.asarray(swapped), vals, n, k, table, 0.0)
+    # a clearly lower score instead of a selected one
+    low = otk.emit_ids(np.r_[order[: k - 1], order[-1]], table)
+    with pytest.raises(AssertionError):
+        otk.check_row_within(np.asarray(low), vals, n, k, table, tol)
+    # a duplicate, a hole (-1 inside), a position past the prefix
+    dup = np.asarray(good).copy(); dup[1] = dup[0]
+    hole = np.asarray(good).copy(); hole[3] = -1
+    with pytest.raises(AssertionError):
+        otk.check_row_within(dup, vals, n, k, table, tol)
+    with pytest.raises(AssertionError):
+        otk.check_row_within(hole, vals, n, k, table, tol)
+    with pytest.raises(AssertionError):
+        otk.check_row_within(np.asarray(good), vals, 100, k, table, tol)
