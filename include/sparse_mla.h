@@ -19,17 +19,24 @@
  * Work is split in three calls, all asynchronous on the caller's CUDA stream:
  *   1. sparse_mla_sched_meta  -- greedy split-KV partition plan, computed on the GPU
  *   2. sparse_mla_decode_fwd  -- gather + dequant + QK^T + online softmax + PV
+ *      (sparse_mla_decode_fwd_ex: with the attention sink, per-token top-k lengths, bf16
+ *      split partials or a second KV cache)
  *   3. sparse_mla_combine     -- LSE-weighted merge of the split partial results
+ * The steps that produce the index list are here too:
+ *   sparse_mla_indexer_scores   -- the lightning-indexer scores over a paged FP8 key cache
+ *   sparse_mla_topk_page_table  -- their exact top-k, emitted as physical cache ids
+ *   sparse_mla_indexer_topk     -- the two chained, without the full score matrix
  *
  * Conventions shared by every entry point:
- *   - All buffers are owned by the caller.  The library allocates no memory, keeps no
- *     global state and never synchronises a stream, except sparse_mla_read_device_status.
+ *   - All buffers are owned by the caller.  The library allocates no memory and keeps no
+ *     global state (except the fixed static scratch of sparse_mla_decode_static), and never
+ *     synchronises a stream, except sparse_mla_read_device_status.
  *   - Pointers marked "device" must be device-accessible memory on the current device.
  *   - Arguments are validated before anything is launched; a bad argument returns an error
  *     and launches nothing.  The library never aborts the process and never prints.
  *   - A failed CUDA launch returns SMLA_ERR_CUDA (cudaGetLastError is read and cleared).
  *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).
- *   - The same smla_dims and num_sms must be used for the three calls of one problem.
+ *   - The same smla_dims and num_sms must be used for the three decode calls of a problem.
  */
 #ifndef SPARSE_MLA_H_
 #define SPARSE_MLA_H_
