@@ -358,8 +358,8 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* dims, int num_sms
 /*
  * sparse_mla_indexer_topk -- the two selection steps chained, without the [n_tok][ld] score
  * matrix ("FlashMLA 与 DSA", sections 4.1, 5.3 and 5.5; "sparse-attention co-design",
- * section 5, steps one to five: the indexer scores feed the top-k and only the selected ids
- * are kept).  For each run of query tokens whose scores fit `scratch`, the indexer scores
+ * section 5, steps one to five, and its summary, which proposes fusing the indexer with the
+ * top-k so that the full fp32 scores are neither written back nor read again).  For each run of query tokens whose scores fit `scratch`, the indexer scores
  * (as sparse_mla_indexer_scores) go into scratch and the exact top-k with the page-table emit
  * (as sparse_mla_topk_page_table on fp32 scores) reads them back, so the scores of at most
  * scratch_bytes / (L * 4) tokens exist at a time; with the scratch the size helper returns
