@@ -89,8 +89,12 @@ typedef struct {
  * sparse_mla_workspace_size -- sizes of the two caller-owned device buffers.
  *   num_sms      SMs the plan may use; <= 0 means "all SMs of the current device".
  *   sched_bytes  out: bytes for the partition plan (sparse_mla_sched_meta writes it).
- *   accum_bytes  out: bytes for the split-partial workspace (fp32 partial O and base-2 lse
- *                of at most b + num_sm_parts splits per query position).
+ *   accum_bytes  out: bytes for the split-partial workspace: fp32 partial O [slots][s_q]
+ *                [h_q][512], then (256-byte aligned) base-2 lse [slots][s_q][h_q], where
+ *                slots = num_splits[r + 1] for the last request r that the plan splits.  0
+ *                when the plan splits no request (the workspace pointer may then be NULL).
+ *                The plan is a pure function of (b, topk, extra_topk, num_sms), walked here
+ *                on the host in O(num_sm_parts).
  * Host-only; launches nothing.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED,
  * SMLA_ERR_CUDA (device query failed).
  */
@@ -130,7 +134,8 @@ smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sche
  *              example -1) masks the slot; a repeated id counts once per slot
  *   sm_scale   softmax scale applied to q.K (for example 1/sqrt(576))
  *   sched_meta device, the plan written by sparse_mla_sched_meta for the same dims/num_sms
- *   workspace  device, >= accum_bytes, 16-byte aligned: split partials (read by combine)
+ *   workspace  device, >= accum_bytes, 16-byte aligned: split partials (read by combine);
+ *              may be NULL when accum_bytes is 0
  *   out        device bf16 [b][s_q][h_q][512], 16-byte aligned; rows of unsplit requests
  *              are final after this call, split rows after sparse_mla_combine
  *   lse        device fp32 [b][h_q][s_q] (note the axis order), natural log, +inf for a
@@ -241,18 +246,28 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
  *     device, created when the library's CUDA module loads; the call allocates nothing.
  *     A problem whose plan plus split partials (sparse_mla_workspace_size) exceed it is
  *     rejected with SMLA_ERR_WORKSPACE before anything is launched.  With num_sms = 152
- *     that admits, for example, b = 64, s_q = 1, h_q = 128 (37 MB) and b = 128, s_q = 2,
- *     h_q = 64 (44 MB); use the three-call sequence with caller buffers beyond that.
+ *     that admits, for example, b = 64, s_q = 1, h_q = 128 and b = 1, s_q = 4096,
+ *     h_q = 128 (no request split: only the plan), b = 32, s_q = 1, h_q = 128 (every
+ *     request split in two: 16 MB) and b = 128, s_q = 2, h_q = 64; use the three-call
+ *     sequence with caller buffers beyond that.
+ *   - The array belongs to the library's CUDA module, so every process that loads the
+ *     module on a device holds its 48 MiB there until exit, whether or not it calls this
+ *     entry point; under lazy module loading (the CUDA default) that happens on the first
+ *     launch of any kernel of the library, under CUDA_MODULE_LOADING=EAGER when the library
+ *     initialises CUDA on the device.
  *   - The first call on a device, made with that device current, looks up the array's
- *     device address (cudaGetSymbolAddress, which may load the CUDA module) and caches it;
- *     make that first call before any stream capture begins.
+ *     device address (cudaGetSymbolAddress, which may load the CUDA module) and caches it
+ *     for the current CUDA context; make that first call before any stream capture begins.
+ *     A device reset (cudaDeviceReset, or a primary-context release and re-creation) ends
+ *     the context the address belongs to: the next call sees the new context's id and
+ *     looks the address up again, so that call too should come before any stream capture.
  *   - Every call on a device uses the same scratch, so two calls whose executions overlap
  *     on the GPU (different streams without an ordering between them, or host threads
  *     issuing at the same time) corrupt each other's results.  Order them, for example by
  *     issuing all of them on one stream.
  *   - The planner zeroes the status words at the start of every call and nothing else in
- *     the scratch needs an initial value; the device status of the last call cannot be
- *     read back through sparse_mla_read_device_status (its plan is not caller-visible).
+ *     the scratch needs an initial value.  The device status word of the last call (a wait
+ *     that ran out, the input range flags) is read with sparse_mla_static_read_status.
  * Asynchronous on stream.  Errors: as sparse_mla_decode_fwd, plus SMLA_ERR_WORKSPACE for a
  * problem above the scratch size and SMLA_ERR_CUDA if the address lookup fails.
  */
@@ -260,6 +275,17 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
 smla_status sparse_mla_decode_static(const smla_dims* dims, int num_sms, const void* q,
                                      const void* kv_cache, const int32_t* indices,
                                      float sm_scale, void* out, float* lse, void* stream);
+
+/*
+ * sparse_mla_static_read_status -- the device status word of the last sparse_mla_decode_static
+ * call on the current device with these dims and num_sms (the word lives in the plan, inside
+ * the library's scratch).  Same results as sparse_mla_read_device_status: *code = the word,
+ * SMLA_OK when it is 0, SMLA_ERR_TIMEOUT when SMLA_DEV_TIMEOUT is set, SMLA_ERR_DEVICE for
+ * any other bit.  Synchronises stream (the read is ordered after the work issued on it).
+ * The pages describe no such call.  Errors: as sparse_mla_decode_static before its launches.
+ */
+smla_status sparse_mla_static_read_status(const smla_dims* dims, int num_sms, int* code,
+                                          void* stream);
 
 /*
  * sparse_mla_plan_has_splits -- whether the plan of these sizes splits any request across
@@ -373,7 +399,9 @@ smla_status sparse_mla_indexer_scores(const smla_indexer_dims* dims, int num_sms
  *   scratch          device buffer, 16-byte aligned, at least L * 4 bytes (one token's
  *                    scores); its contents on return are unspecified
  *   out_indices      device int32 [n_tok][topk] (written), as for sparse_mla_topk_page_table
- *   status           optional device uint32 word (SMLA_DEV_TIMEOUT, SMLA_DEV_TOPK_TABLE)
+ *   status           device uint32 word, required (SMLA_DEV_TIMEOUT, SMLA_DEV_TOPK_TABLE are
+ *                    or-ed in): the top-k of a run reads the scores its indexer launch left,
+ *                    so a wait that ran out in the indexer must be visible to the caller
  * Launches two kernels per run of tokens, all on stream, asynchronously.  Errors:
  * SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED, SMLA_ERR_ALIGNMENT (also ld not a multiple of
  * 4), SMLA_ERR_WORKSPACE (scratch below one token's scores), SMLA_ERR_CUDA.

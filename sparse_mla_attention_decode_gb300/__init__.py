@@ -19,7 +19,8 @@ __all__ = [
     "SMLA_OK", "SparseMLAError", "smla_dims", "lib", "build", "library_path",
     "sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
     "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
-    "sparse_mla_version", "sparse_mla_decode_static", "STATIC_SCRATCH_BYTES",
+    "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_static_read_status",
+    "STATIC_SCRATCH_BYTES",
     "smla_decode_opts", "sparse_mla_decode_fwd_ex", "sparse_mla_combine_ex",
     "sparse_mla_plan_has_splits", "smla_topk_dims", "sparse_mla_topk_page_table",
     "topk_page_table", "SMLA_SCORES_BF16", "SMLA_SCORES_FP32",
@@ -43,7 +44,7 @@ EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_de
             "sparse_mla_version", "sparse_mla_decode_static", "sparse_mla_decode_fwd_ex",
             "sparse_mla_combine_ex", "sparse_mla_plan_has_splits", "sparse_mla_topk_page_table",
             "sparse_mla_indexer_scores", "sparse_mla_indexer_topk_scratch_size",
-            "sparse_mla_indexer_topk"]
+            "sparse_mla_indexer_topk", "sparse_mla_static_read_status"]
 # Scratch budget of the chained selection (SMLA_SELECT_SCRATCH_BUDGET): scores kept in L2.
 SELECT_SCRATCH_BUDGET = 48 << 20
 # Size of the library-owned scratch of sparse_mla_decode_static (SMLA_STATIC_SCRATCH_BYTES).
@@ -130,6 +131,8 @@ def lib():
             L.sparse_mla_version.restype = ctypes.c_char_p
             L.sparse_mla_decode_static.argtypes = [P(smla_dims), ctypes.c_int, vp, vp, vp,
                                                    ctypes.c_float, vp, vp, vp]
+            L.sparse_mla_static_read_status.argtypes = [P(smla_dims), ctypes.c_int,
+                                                        P(ctypes.c_int), vp]
             for f in EXPORTED:
                 if f not in ("sparse_mla_status_string", "sparse_mla_version"):
                     getattr(L, f).restype = ctypes.c_int
@@ -215,6 +218,15 @@ def sparse_mla_decode_static(dims: smla_dims, num_sms: int, q: int, kv_cache: in
         raise SparseMLAError(rc, f"sparse_mla_decode_static: the problem needs {need} bytes of "
                                  f"scratch, the fixed scratch holds {STATIC_SCRATCH_BYTES}")
     _check(rc, "sparse_mla_decode_static")
+
+
+def sparse_mla_static_read_status(dims: smla_dims, num_sms: int, stream: int = 0) -> tuple[int, int]:
+    """(status code of the call, device status word) of the last sparse_mla_decode_static call
+    with these sizes on the current device."""
+    code = ctypes.c_int()
+    rc = lib().sparse_mla_static_read_status(ctypes.byref(dims), int(num_sms), ctypes.byref(code),
+                                             stream)
+    return rc, code.value
 
 
 def sparse_mla_plan_has_splits(dims: smla_dims, num_sms: int) -> bool:
@@ -326,11 +338,13 @@ def indexer_topk(q8, weights, k_cache, block_table, valid_len, s_q: int, ld: int
         raise ValueError("scratch must be contiguous")
     if out is None:
         out = torch.empty(n_tok, k, dtype=torch.int32, device=q8.device)
+    if status is None:  # the chained call needs a status word; this one is not read back
+        status = torch.zeros(1, dtype=torch.int32, device=q8.device)
     st = (stream if stream is not None else torch.cuda.current_stream(q8.device)).cuda_stream
     sparse_mla_indexer_topk(d, k, num_sms, q8.data_ptr(), weights.data_ptr(), k_cache.data_ptr(),
                             block_table.data_ptr(), valid_len.data_ptr(), scratch.data_ptr(),
                             scratch.numel() * scratch.element_size(), out.data_ptr(),
-                            status.data_ptr() if status is not None else 0, st)
+                            status.data_ptr(), st)
     return out
 
 

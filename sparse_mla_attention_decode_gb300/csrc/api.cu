@@ -82,20 +82,46 @@ smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
   return SMLA_OK;
 }
 
-// Whether the greedy plan of these sizes splits any request, in closed form.  Every request has
-// the same nb = ceil(topk / 64) blocks and costs c = nb + 5, every partition has the same
-// payload P = ceil(b c / parts) + 5.  The first partition takes k = floor(P / c) whole requests
-// and then splits the next one exactly when more than the overhead of 5 is left (P mod c > 5,
-// which includes P < c) and a request is left (b > k).  A partition that closes at a request
-// boundary leaves the next one starting the same way, so either the first partition splits a
-// request or no partition does.
-bool plan_splits(int64_t b, int64_t topk, int parts) {
-  const int64_t nb = (static_cast<int64_t>(topk) + kPage - 1) / kPage;
-  if (b <= 0 || nb <= 0) return false;
+// Split slots the workspace must hold: the plan numbers the splits of request r from
+// prefix[r] = r + (number of partitions that start inside an earlier request), so the last
+// request that is split (one that a partition starts inside) ends at slot r_last + 1 +
+// (partitions that start inside a request), and no slot past it is ever written.  0 when no
+// request is split.  The same greedy walk as the planner kernel, one partition per step with
+// the whole requests of a step taken at once: O(parts).
+int64_t split_slots(int64_t b, int64_t topk, int parts) {
+  const int64_t nb = (topk + kPage - 1) / kPage;
+  if (b <= 0 || nb <= 0) return 0;
   const int64_t c = nb + kFixedOverhead;
   const int64_t P = (b * c + parts - 1) / parts + kFixedOverhead;
-  const int64_t k = P / c;
-  return P - k * c > kFixedOverhead && b > k;
+  int64_t req = 0, blk = 0, mid_starts = 0, last_split = -1;
+  for (int p = 0; p < parts && req < b; ++p) {
+    if (blk > 0) {  // this partition starts inside request req: req is split
+      ++mid_starts;
+      last_split = req;
+    }
+    int64_t remain = P;
+    const int64_t left = nb - blk;
+    if (left + kFixedOverhead <= remain) {  // the rest of the current request fits
+      remain -= left + kFixedOverhead;
+      ++req;
+      blk = 0;
+      if (remain > kFixedOverhead && req < b) {
+        int64_t whole = remain / c;  // c > 5, so a request that fits leaves remain > 5 first
+        if (whole > b - req) whole = b - req;
+        remain -= whole * c;
+        req += whole;
+        if (req < b && remain > kFixedOverhead) blk = remain - kFixedOverhead;  // split here
+      }
+    } else {
+      blk += remain - kFixedOverhead;  // take what fits and split the request here
+    }
+  }
+  return last_split < 0 ? 0 : last_split + 1 + mid_starts;
+}
+
+AccumLayout workspace_layout(const smla_dims* d, int parts) {
+  const int64_t slots = split_slots(d->b, plan_topk(d), parts);
+  return accum_layout_slots(static_cast<int>(slots), d->s_q, d->h_q);
 }
 
 smla_status cuda_status(cudaError_t e) {
@@ -165,7 +191,7 @@ smla_status sparse_mla_workspace_size(const smla_dims* dims, int num_sms, size_t
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
   *sched_bytes = plan_layout(dims->b, parts).bytes;
-  *accum_bytes = accum_layout(dims->b, dims->s_q, dims->h_q, parts).bytes;
+  *accum_bytes = workspace_layout(dims, parts).bytes;
   return SMLA_OK;
 }
 
@@ -208,7 +234,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   if (st != SMLA_OK) return st;
   const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
   if (tokens == 0) return SMLA_OK;
-  if (!q || !sched_meta || !out || !lse || !workspace) return SMLA_ERR_INVALID_ARG;
+  if (!q || !sched_meta || !out || !lse) return SMLA_ERR_INVALID_ARG;
   if (dims->topk > 0 && (!indices || (dims->num_blocks > 0 && !kv_cache))) return SMLA_ERR_INVALID_ARG;
   const bool extra = dims->extra_topk > 0;
   if (extra && (!opts || !opts->extra_indices ||
@@ -221,7 +247,8 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   if ((st = check_opts(opts)) != SMLA_OK) return st;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
-  const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
+  const AccumLayout A = workspace_layout(dims, parts);
+  if (A.bytes > 0 && !workspace) return SMLA_ERR_INVALID_ARG;
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (plan_topk(dims) == 0)
@@ -231,21 +258,28 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   const uint8_t* plan = static_cast<const uint8_t*>(sched_meta);
   DecodeParams p;
   if (!encode_rows_map(&p.q_map, q, false, tokens * dims->h_q, kDQk, 64, dims->h_q) ||
-      !encode_rows_map(&p.out_map, out, false, tokens * dims->h_q, kDV, 64, dims->h_q) ||
-      !encode_rows_map(&p.acc_map, static_cast<uint8_t*>(workspace) + A.o_off, true,
-                       static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q, kDV, 32,
-                       dims->h_q) ||
-      !encode_rows_map(&p.acc16_map, static_cast<uint8_t*>(workspace) + A.o_off, false,
-                       static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q, kDV, 64,
-                       dims->h_q))
+      !encode_rows_map(&p.out_map, out, false, tokens * dims->h_q, kDV, 64, dims->h_q))
     return SMLA_ERR_CUDA;
+  if (A.max_splits > 0) {
+    uint8_t* acc = static_cast<uint8_t*>(workspace) + A.o_off;
+    const int64_t rows = static_cast<int64_t>(A.max_splits) * dims->s_q * dims->h_q;
+    if (!encode_rows_map(&p.acc_map, acc, true, rows, kDV, 32, dims->h_q) ||
+        !encode_rows_map(&p.acc16_map, acc, false, rows, kDV, 64, dims->h_q))
+      return SMLA_ERR_CUDA;
+  } else {  // no split slot: the kernel stores no partial, so these maps are never used
+    p.acc_map = p.out_map;
+    p.acc16_map = p.out_map;
+  }
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.kv = static_cast<const uint8_t*>(kv_cache);
   p.indices = indices;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.o_accum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.o_off);
-  p.lse_accum = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.lse_off);
+  p.o_accum = A.max_splits > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.o_off)
+                               : nullptr;
+  p.lse_accum = A.max_splits > 0
+                    ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + A.lse_off)
+                    : nullptr;
   p.meta = reinterpret_cast<const int32_t*>(plan + L.meta_off);
   p.nsplits = reinterpret_cast<const int32_t*>(plan + L.prefix_off);
   p.status = const_cast<uint32_t*>(reinterpret_cast<const uint32_t*>(plan + L.status_off));
@@ -265,7 +299,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.nb_main = (dims->topk + kPage - 1) / kPage;
   p.nb_total = static_cast<int>((plan_topk(dims) + kPage - 1) / kPage);
   p.num_rows = static_cast<int>(dims->num_blocks * kPage);
-  p.store32 = aligned(out, 32) && aligned(workspace, 32) ? 1 : 0;
+  p.store32 = aligned(out, 32) && (A.max_splits == 0 || aligned(workspace, 32)) ? 1 : 0;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 / 256.0);
   return cuda_status(launch_decode(p, parts, s));
 }
@@ -285,16 +319,17 @@ smla_status sparse_mla_combine_ex(const smla_dims* dims, int num_sms,
   if (st != SMLA_OK) return st;
   const int64_t tokens = static_cast<int64_t>(dims->b) * dims->s_q;
   if (tokens == 0 || plan_topk(dims) == 0) return SMLA_OK;
-  if (!sched_meta || !workspace || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (!sched_meta || !out || !lse) return SMLA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(workspace, 16) || !aligned(sched_meta, 16) || !aligned(lse, 4))
     return SMLA_ERR_ALIGNMENT;
   if ((st = check_opts(opts)) != SMLA_OK) return st;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
-  const AccumLayout A = accum_layout(dims->b, dims->s_q, dims->h_q, parts);
+  const AccumLayout A = workspace_layout(dims, parts);
+  if (A.bytes > 0 && !workspace) return SMLA_ERR_INVALID_ARG;
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
   // no request is split: the decode pass wrote every row, so nothing is launched
-  if (!plan_splits(dims->b, plan_topk(dims), parts)) return SMLA_OK;
+  if (A.max_splits == 0) return SMLA_OK;
   const PlanLayout L = plan_layout(dims->b, parts);
   CombineParams p;
   p.o_accum = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + A.o_off);
@@ -423,7 +458,8 @@ smla_status sparse_mla_indexer_topk(const smla_indexer_dims* d, int32_t topk, in
   if (d->heads != 64 || d->dim != 128) return SMLA_ERR_UNSUPPORTED;
   if (d->n_tok % d->s_q != 0) return SMLA_ERR_INVALID_ARG;
   if (d->n_tok == 0) return SMLA_OK;
-  if (!scratch || !out_indices || !q8 || !weights || !block_table || !valid_len) return SMLA_ERR_INVALID_ARG;
+  if (!scratch || !out_indices || !q8 || !weights || !block_table || !valid_len || !status)
+    return SMLA_ERR_INVALID_ARG;
   if (d->ld % 4 != 0 || !aligned(scratch, 16)) return SMLA_ERR_ALIGNMENT;
   const int64_t row = L * 4;
   if (row > 0 && scratch_bytes < static_cast<size_t>(row)) return SMLA_ERR_WORKSPACE;
@@ -473,7 +509,7 @@ smla_status sparse_mla_plan_has_splits(const smla_dims* dims, int num_sms, int* 
   if (!has_splits) return SMLA_ERR_INVALID_ARG;
   int parts = 0;
   if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
-  *has_splits = plan_splits(dims->b, plan_topk(dims), parts) ? 1 : 0;
+  *has_splits = split_slots(dims->b, plan_topk(dims), parts) > 0 ? 1 : 0;
   return SMLA_OK;
 }
 

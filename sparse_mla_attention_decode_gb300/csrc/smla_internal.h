@@ -29,19 +29,21 @@ inline PlanLayout plan_layout(int b, int parts) {
   L.bytes = L.status_off + 64;
   return L;
 }
-// Layout of the split-partial workspace: o_accum fp32 [max_splits][s_q][h_q][512] then
-// lse_accum fp32 [max_splits][s_q][h_q] (base-2 log-sum-exp).
+// Layout of the split-partial workspace: o_accum fp32 [slots][s_q][h_q][512] then lse_accum
+// fp32 [slots][s_q][h_q] (base-2 log-sum-exp), where slots is the number of split slots the
+// plan numbers up to its last split request (split_slots); a plan that splits no request
+// needs no workspace at all.
 struct AccumLayout {
   int max_splits;
   size_t o_off, lse_off, bytes;
 };
-inline AccumLayout accum_layout(int b, int s_q, int h_q, int parts) {
+inline AccumLayout accum_layout_slots(int slots, int s_q, int h_q) {
   AccumLayout L;
-  L.max_splits = b + parts;
+  L.max_splits = slots;
   L.o_off = 0;
-  size_t o_bytes = static_cast<size_t>(L.max_splits) * s_q * h_q * kDV * 4;
+  size_t o_bytes = static_cast<size_t>(slots) * s_q * h_q * kDV * 4;
   L.lse_off = (o_bytes + 255) & ~static_cast<size_t>(255);
-  L.bytes = L.lse_off + static_cast<size_t>(L.max_splits) * s_q * h_q * 4;
+  L.bytes = slots > 0 ? L.lse_off + static_cast<size_t>(slots) * s_q * h_q * 4 : 0;
   return L;
 }
 

@@ -35,6 +35,17 @@ def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True
     return out, lse, op
 
 
+def accum_layout(prefix, s_q: int, h_q: int):
+    """(slots, lse byte offset) of the split-partial workspace of a plan with this num_splits
+    prefix, as include/sparse_mla.h documents it: slots = prefix[r + 1] for the last request r
+    that the plan splits (0 when none is), fp32 partial O [slots][s_q][h_q][512], then the
+    base-2 lse [slots][s_q][h_q] at the next 256-byte boundary."""
+    prefix = [int(x) for x in prefix]
+    split = [r for r in range(len(prefix) - 1) if prefix[r + 1] - prefix[r] > 1]
+    slots = prefix[split[-1] + 1] if split else 0
+    return slots, ((slots * s_q * h_q * 512 * 4) + 255) // 256 * 256
+
+
 def compact_inputs(wl: workloads.Workload, tokens: np.ndarray):
     """Oracle inputs restricted to ``tokens``: the rows those tokens select are gathered (with
     torch, from the seeded inputs) into a small pool and their indices renumbered.  Invalid

@@ -48,7 +48,38 @@ def test_workspace_sizes(L):
     sb, ab = smla.sparse_mla_workspace_size(d, 152)
     parts = 152 // 1 // 2
     assert sb >= parts * 32 + 65 * 4 + 4
-    assert ab >= (64 + parts) * 128 * 512 * 4 + (64 + parts) * 128 * 4
+    assert ab == 0  # this plan splits no request: no split-partial workspace at all
+    # the prefill-shaped problem needs none either (it used to ask for 2 GiB)
+    assert smla.sparse_mla_workspace_size(smla.dims_for(1, 4096, 128, 2048, 1024), 152)[1] == 0
+
+
+def _expected_accum_bytes(b, s_q, h_q, topk, num_sms):
+    """The split-partial workspace as the header documents it, from the oracle's planner:
+    slots = num_splits[r + 1] for the last split request r, fp32 O [slots][s_q][h_q][512],
+    then the base-2 lse [slots][s_q][h_q] at the next 256-byte boundary."""
+    from oracle import sched as osched
+    _, prefix = osched.plan([topk] * b, osched.num_sm_parts(num_sms, s_q))
+    split = [r for r in range(b) if prefix[r + 1] - prefix[r] > 1]
+    if not split:
+        return 0
+    slots = prefix[split[-1] + 1]
+    lse_off = (slots * s_q * h_q * 512 * 4 + 255) // 256 * 256
+    return lse_off + slots * s_q * h_q * 4
+
+
+def test_workspace_size_follows_the_plan(L):
+    """accum_bytes covers exactly the split slots the oracle's planner numbers."""
+    rng = __import__("random").Random(17)
+    cases = [(2, 1, 128, 128, 132), (64, 1, 128, 2048, 152), (32, 1, 128, 2048, 152),
+             (128, 2, 64, 2048, 152), (1, 4096, 128, 2048, 152), (3, 2, 64, 2048, 40),
+             (2, 3, 128, 2048, 60), (1, 1, 128, 2048, 152), (4, 1, 128, 512, 120),
+             (77, 1, 128, 2048, 152), (5, 1, 64, 0, 16), (64, 8, 128, 2048, 152)]
+    cases += [(rng.randint(1, 300), rng.choice([1, 1, 2, 3, 8]), rng.choice([64, 128]),
+               rng.randint(0, 5000), rng.randint(2, 300)) for _ in range(300)]
+    for b, s_q, h_q, topk, num_sms in cases:
+        d = smla.dims_for(b, s_q, h_q, topk, 64)
+        _, ab = smla.sparse_mla_workspace_size(d, num_sms)
+        assert ab == _expected_accum_bytes(b, s_q, h_q, topk, num_sms), (b, s_q, h_q, topk, num_sms)
 
 
 @pytest.mark.parametrize("field,value,code", [("h_q", 96, 2), ("d_qk", 512, 2), ("d_v", 256, 2),
@@ -145,7 +176,8 @@ def test_product_path_does_not_touch_the_oracle():
 
 
 def test_plan_has_splits_matches_oracle_planner(L):
-    """The host-side closed form agrees with the oracle's greedy planner (any request split)."""
+    """The host-side walk of the plan agrees with the oracle's greedy planner (any request
+    split)."""
     from oracle import sched as osched
     rng = __import__("random").Random(5)
     cases = [(2, 1, 128, 132), (64, 1, 2048, 152), (32, 1, 2048, 152), (128, 2, 2048, 152),
@@ -176,7 +208,8 @@ def test_extra_list_needs_its_pointers(L):
     d0 = smla.dims_for(2, 1, 128, 128, 64)
     d3 = smla.dims_for(2, 1, 128, 192, 64)
     assert smla.sparse_mla_plan_has_splits(d, 152) == smla.sparse_mla_plan_has_splits(d3, 152)
-    assert smla.sparse_mla_workspace_size(d, 152) == smla.sparse_mla_workspace_size(d0, 152)
+    assert smla.sparse_mla_workspace_size(d, 152) == smla.sparse_mla_workspace_size(d3, 152)
+    assert smla.sparse_mla_workspace_size(d0, 152)[0] == smla.sparse_mla_workspace_size(d, 152)[0]
 
 
 def test_topk_argument_checks(L):
@@ -207,11 +240,12 @@ def test_indexer_argument_checks(L):
 def test_indexer_topk_argument_checks(L):
     fake = 0x10000
 
-    def call(d, topk=16, scratch=fake, nbytes=1 << 20):
+    def call(d, topk=16, scratch=fake, nbytes=1 << 20, status=fake):
         return L.sparse_mla_indexer_topk(ctypes.byref(d), topk, 152, fake, fake, fake, fake, fake,
-                                         scratch, nbytes, fake, None, None)
+                                         scratch, nbytes, fake, status, None)
     ok = smla.smla_indexer_dims(4, 2, 64, 128, 8, 512, 16)
     assert call(ok, topk=0) == 1                                             # topk
+    assert call(ok, status=None) == 1                                         # status required
     assert call(smla.smla_indexer_dims(4, 1, 32, 128, 8, 512, 16)) == 2       # heads
     assert call(smla.smla_indexer_dims(5, 2, 64, 128, 8, 512, 16)) == 1       # n_tok % s_q
     assert call(ok, scratch=None) == 1                                        # no scratch

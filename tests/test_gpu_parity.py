@@ -3,8 +3,9 @@
 Small cases are compared in full (several pipeline blocks, split and unsplit requests, ragged
 top-k tails, masked / out-of-range / duplicate slots, all-masked rows, h_q = 64 and 128,
 fp32 and power-of-two scales).  The five benchmark workloads run at their full sizes in the
-launch configuration the benchmark uses, and sampled query tokens are compared with the
-oracle computed for those tokens."""
+launch configuration the benchmark uses: every query token of the four decode workloads,
+and a seeded 512-token subset (first and last tokens included) of the prefill-shaped one, is
+compared element by element with the oracle."""
 
 import math
 
@@ -129,14 +130,14 @@ def test_combine_kernel_vs_oracle(dev):
     # the oracle planner's split layout (the GPU plan must equal it)
     _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
     assert op.plan()[1].tolist() == pre
-    max_splits = b + parts
+    max_splits, lse_off = gu.accum_layout(pre, s_q, h)
+    assert max_splits > b and op.accum_bytes == lse_off + max_splits * s_q * h * 4
     g = torch.Generator(device="cpu").manual_seed(4)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)
     l_acc = torch.randn(max_splits, s_q, h, generator=g) * 4
     l_acc[pre[0], 0, :5] = -math.inf                      # some empty splits
     l_acc[pre[1]:pre[2], 1, 7] = -math.inf                # a row whose splits are all empty
     o_off = 0
-    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
     wsb = op.workspace
     wsb[o_off:o_off + o_acc.numel() * 4].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
     wsb[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
@@ -170,10 +171,9 @@ def test_split_partials_match_oracle(dev):
     parts = max(op.num_sms // 1 // 2, 1)
     plan, prefix = osched.plan([256] * 2, parts)
     assert pre.tolist() == prefix
-    max_splits = 2 + parts
+    max_splits, lse_off = gu.accum_layout(prefix, 1, 128)
     ws = op.workspace.cpu()
     o_acc = ws[: max_splits * 128 * 512 * 4].view(torch.float32).view(max_splits, 1, 128, 512)
-    lse_off = ((max_splits * 128 * 512 * 4) + 255) // 256 * 256
     l_acc = ws[lse_off: lse_off + max_splits * 128 * 4].view(torch.float32).view(max_splits, 1, 128)
     q, kv, idx = workloads.to_numpy_inputs(wl)
     checked = 0
@@ -196,10 +196,20 @@ def test_split_partials_match_oracle(dev):
 
 # ----------------------------------------------------------------------------- full-size workloads
 
-def _sample_tokens(n_tok, k, seed):
-    rng = np.random.default_rng(seed)
-    pick = set([0, n_tok - 1])
-    while len(pick) < min(k, n_tok):
+# Query tokens compared per full-size workload: all of them, except for the prefill-shaped one
+# (4096 tokens x 128 heads x 2048 slots is about 2.3 TFLOP of fp64), where a seeded subset of
+# 512 tokens that always holds the first and the last token (the shortest and the longest
+# causal prefix) is compared.
+C5_SUBSET = 512
+
+
+def parity_tokens(spec) -> np.ndarray:
+    n_tok = spec.b * spec.s_q
+    if n_tok <= C5_SUBSET:
+        return np.arange(n_tok)
+    rng = np.random.default_rng(1000 + spec.seed)
+    pick = {0, n_tok - 1}
+    while len(pick) < C5_SUBSET:
         pick.add(int(rng.integers(0, n_tok)))
     return np.array(sorted(pick))
 
@@ -210,12 +220,13 @@ def test_benchmark_workload_parity(dev, cfg):
     wl = workloads.make(spec, device=dev)
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out, lse, _ = gu.run_cuda(wl, num_sms=num_sms)
-    n_tok = spec.b * spec.s_q
-    # properties at any size: finite outputs, finite lse on rows with a valid slot
-    assert torch.isfinite(out.float()).all()
-    assert torch.isfinite(lse).all()
-    tokens = _sample_tokens(n_tok, 24 if n_tok > 24 else n_tok, spec.seed)
+    tokens = parity_tokens(spec)
     ro, rl = gu.oracle_tokens(wl, tokens)
     go, gl = gu.gpu_tokens(out, lse, wl, tokens)
     m = gu.compare(go, gl, ro, rl, cfg)
-    print(cfg, m)
+    print(f"PARITY {cfg} tokens={len(tokens)}/{spec.b * spec.s_q} max_abs={m['max_abs']:.3e} "
+          f"rel_l2={m['rel_l2']:.3e} worst_row_rel={m['worst_row_rel']:.3e} "
+          f"lse_abs={m['lse_abs']:.3e}")
+    if len(tokens) < spec.b * spec.s_q:
+        # tokens outside the compared subset: finite, and every row has a valid slot
+        assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()

@@ -1,7 +1,7 @@
 """GPU parity of the decode variants (attention sink, per-token top-k length) through the C
 ABI against the fp64 oracle: small cases in full on unsplit and split plans, the combine
 kernel with a sink on synthetic partials, and the full-size b=64 / h=128 / topk=2048
-workload with both variants on sampled tokens."""
+workload with both variants on every query token."""
 
 import math
 
@@ -82,7 +82,7 @@ def test_combine_kernel_with_sink(dev):
     # the oracle planner's split layout (the GPU plan must equal it)
     _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
     assert op.plan()[1].tolist() == pre
-    max_splits = b + parts
+    max_splits, lse_off = gu.accum_layout(pre, s_q, h)
     g = torch.Generator(device="cpu").manual_seed(14)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g)
     l_acc = torch.randn(max_splits, s_q, h, generator=g) * 4 + 6
@@ -90,7 +90,6 @@ def test_combine_kernel_with_sink(dev):
     sink = workloads.attn_sink(h, 3)
     sink[5] = 60.0   # far above every lse: output about 0
     sink[6] = -60.0  # far below: no effect
-    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
     ws = op.workspace
     ws[: o_acc.numel() * 4].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
     ws[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
@@ -129,9 +128,7 @@ def test_full_size_workload_with_variants(dev):
     sink = workloads.attn_sink(spec.h_q, 77, device=dev)
     lens = workloads.topk_lengths(spec.b, spec.s_q, spec.topk, 77, device=dev)
     out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, attn_sink=sink, topk_length=lens)
-    assert torch.isfinite(out.float()).all()
-    tokens = np.array(sorted(set([0, 1, 2, 3, 4, 5, 6, 63] +
-                                 list(np.random.default_rng(7).integers(0, 64, 12)))))
+    tokens = np.arange(spec.b * spec.s_q)  # every query token
     ro, rl = gu.oracle_tokens(wl, tokens, attn_sink=sink, topk_length=lens)
     go, gl = gu.gpu_tokens(out, lse, wl, tokens)
     print(gu.compare(go, gl, ro, rl, "c2 with sink and lengths"))
@@ -183,12 +180,11 @@ def test_combine_kernel_bf16_partials(dev):
     # the oracle planner's split layout (the GPU plan must equal it)
     _, pre = osched.plan([2048] * b, osched.num_sm_parts(op.num_sms, s_q))
     assert op.plan()[1].tolist() == pre
-    max_splits = b + parts
+    max_splits, lse_off = gu.accum_layout(pre, s_q, h)
     g = torch.Generator(device="cpu").manual_seed(15)
     o_acc = torch.randn(max_splits, s_q, h, 512, generator=g).to(torch.bfloat16)
     l_acc = torch.randn(max_splits, s_q, h, generator=g) * 3
     l_acc[pre[0], 1, :9] = -math.inf
-    lse_off = ((max_splits * s_q * h * 512 * 4) + 255) // 256 * 256
     ws = op.workspace
     ws[: o_acc.numel() * 2].copy_(o_acc.view(torch.uint8).view(-1).to(dev))
     ws[lse_off:lse_off + l_acc.numel() * 4].copy_(l_acc.contiguous().view(torch.uint8).view(-1).to(dev))
@@ -281,8 +277,7 @@ def test_full_size_workload_with_extra_kv(dev):
     ekv, eidx = _extra_inputs(wl, 512, ctx=4096, seed=991, masked=20, out_of_range=2)
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out, lse, _ = gu.run_cuda(wl, num_sms=num_sms, extra_kv=ekv, extra_indices=eidx)
-    assert torch.isfinite(out.float()).all()
-    tokens = np.array([0, 1, 17, 31, 32, 50, 62, 63])
+    tokens = np.arange(spec.b * spec.s_q)  # every query token
     ro, rl = gu.oracle_tokens_extra(wl, tokens, ekv, eidx)
     go, gl = gu.gpu_tokens(out, lse, wl, tokens)
     print(gu.compare(go, gl, ro, rl, "c2 with a 512-slot extra list"))

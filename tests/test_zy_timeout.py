@@ -95,3 +95,31 @@ def test_indexer_bounded_wait_runs_out_and_the_context_stays_usable(cuda_ok):
         n = int(lens[t])
         tol = 2e-5 * max(1.0, float(np.abs(ref[t, :n]).max())) + 1e-6
         assert float(np.abs(g[t, :n] - ref[t, :n]).max()) <= tol
+
+
+def test_chained_selection_reports_an_indexer_timeout(cuda_ok):
+    # the chained indexer -> top-k call with the indexer's stall hook: the indexer's waits run
+    # out, the top-k then selects from whatever the scratch holds, and the required status word
+    # carries SMLA_DEV_TIMEOUT, so the caller sees that the ids are not valid; the next chained
+    # call on the same context is clean
+    dev = torch.device("cuda:0")
+    b, pages, ld, k = 2, 40, 2560, 64
+    cache = workloads.indexer_cache(pages, seed=92, device=dev)
+    q8, w = workloads.indexer_queries(b, seed=93, device=dev)
+    table = torch.arange(pages, dtype=torch.int32, device=dev).view(1, pages).repeat(b, 1).contiguous()
+    lens = torch.tensor([ld, 1000], dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(b, k, dtype=torch.int32, device=dev)
+    d = smla.smla_indexer_dims(b, 1, 64, 128, pages, ld, pages)
+    d.test_stall = 1
+    scratch = torch.empty(smla.sparse_mla_indexer_topk_scratch_size(d), dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    smla.sparse_mla_indexer_topk(d, k, 8, q8.data_ptr(), w.data_ptr(), cache.data_ptr(),
+                                 table.data_ptr(), lens.data_ptr(), scratch.data_ptr(),
+                                 scratch.numel(), out.data_ptr(), status.data_ptr(), st)
+    torch.cuda.synchronize()
+    assert int(status.item()) & smla.SMLA_DEV_TIMEOUT
+    status.zero_()
+    smla.indexer_topk(q8, w, cache, table, lens, 1, ld, k, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
