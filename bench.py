@@ -33,7 +33,9 @@ FLUSH_NOTE = ("flushed between steps (256 MiB write, then a 256 MiB read of anot
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse MLA decode TFLOPS & gathered KV tokens/s, % of roofline (1×GB300)"
-DEFAULT_WORKLOAD = "c2_b64_h128_k2048_mask5"
+# The headline is the largest single-GPU workload of the five (the prefill-shaped one, 2.3
+# TFLOP a step); the other four are measured in the same run and reported under per_config.
+DEFAULT_WORKLOAD = "c5_b1_sq4096_h128_k2048"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -234,6 +236,120 @@ def time_oracle(wl, budget_s: float, max_tokens: int | None = None):
     flops = 2.0 * wl.spec.h_q * (workloads.D_QK + workloads.D_V) * valid
     return {"flops": flops, "seconds": elapsed, "tokens": done, "valid_slots": valid,
             "threads": oracle.max_threads(), "passes": done / limit, "pool": limit}
+
+
+def roofline_of(wl, t_dec: float, peaks) -> dict:
+    """The decode kernel against its roofline: T_roof = max(valid-slot FLOPs / bf16 tensor peak,
+    algorithmic bytes / HBM bandwidth); frac = T_roof / measured time; bound = the larger."""
+    import workloads
+    flops = workloads.flops_valid(wl)
+    alg = workloads.alg_bytes(wl)
+    t_tensor = flops / (float(peaks["bf16_tflops"]) * 1e12)
+    t_hbm = alg / (float(peaks["hbm_gbs"]) * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    return {"bound": bound, "t_roof_us": max(t_tensor, t_hbm) * 1e6,
+            "frac": max(t_tensor, t_hbm) / t_dec,
+            "tflops": flops / t_dec / 1e12, "hbm_gbs": alg / t_dec / 1e9,
+            "tensor_frac": t_tensor / t_dec, "hbm_frac": t_hbm / t_dec}
+
+
+def measure_decode(spec, wl, dev, steps: int, warmup: int, flush, gpu_index: int,
+                   barrier=None):
+    """Time plan + decode + combine (one step) and the decode kernel alone on one workload with
+    CUDA events on the launching stream, L2 flushed before every step (outside the events),
+    nvidia-smi clocks sampled during the timed region.  Returns a dict of raw times, the op and
+    the output buffers."""
+    import torch
+
+    import sparse_mla_attention_decode_gb300 as smla
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    op = smla.SparseMLADecode(spec.b, spec.s_q, spec.h_q, spec.topk, wl.kv.shape[0], device=dev,
+                              num_sms=num_sms)
+    out = torch.empty(spec.b, spec.s_q, spec.h_q, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(spec.b, spec.h_q, spec.s_q, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st = stream.cuda_stream
+    d = op.dims
+
+    def sched():
+        smla.sparse_mla_sched_meta(d, num_sms, op.sched.data_ptr(), op.sched_bytes, st)
+
+    def decode():
+        smla.sparse_mla_decode_fwd(d, num_sms, wl.q.data_ptr(), wl.kv.data_ptr(),
+                                   wl.indices.data_ptr(), wl.sm_scale, op.sched.data_ptr(),
+                                   op.workspace.data_ptr(), op.accum_bytes, out.data_ptr(),
+                                   lse.data_ptr(), st)
+
+    def combine():
+        smla.sparse_mla_combine(d, num_sms, op.sched.data_ptr(), op.workspace.data_ptr(),
+                                op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
+
+    launches_per_step = 3 if smla.sparse_mla_plan_has_splits(d, num_sms) else 2
+
+    # One step = plan + decode + combine, back to back on the stream (events only around the
+    # whole step, so the launches overlap as they do in use).
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sched()
+        decode()
+        combine()
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize(dev)
+    if op.device_status() != 0:
+        raise RuntimeError(f"{spec.name}: device status word set during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    dec_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    sampler = ClockSampler(gpu_index)
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        flush(k)
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    # the decode kernel alone (for the roofline): events on the launching stream around it
+    for k in range(steps):
+        flush(k)
+        sched()
+        dec_evs[k][0].record(stream)
+        decode()
+        dec_evs[k][1].record(stream)
+        combine()
+    torch.cuda.synchronize(dev)
+    if barrier is not None:
+        barrier()
+    clocks = sampler.stop()
+    if op.device_status() != 0:
+        raise RuntimeError(f"{spec.name}: device status word set during the timed steps")
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[0].elapsed_time(e[1]) for e in dec_evs]
+    return {"op": op, "out": out, "lse": lse, "step_ms": step_ms, "dec_ms": dec_ms,
+            "wall": wall, "clocks": clocks, "launches_per_step": launches_per_step}
+
+
+def per_config_entry(spec, wl, r, peaks) -> dict:
+    import workloads
+    t_step = sum(r["step_ms"]) / len(r["step_ms"]) / 1e3
+    t_dec = sum(r["dec_ms"]) / len(r["dec_ms"]) / 1e3
+    rf = roofline_of(wl, t_dec, peaks)
+    return {"step_us": t_step * 1e6, "decode_us": t_dec * 1e6,
+            "step_tflops": workloads.flops_valid(wl) / t_step / 1e12,
+            "decode_tflops": rf["tflops"], "decode_hbm_gbs": rf["hbm_gbs"],
+            "gathered_tokens_per_s": wl.num_valid / t_step,
+            "roofline": {"bound": rf["bound"], "t_roof_us": rf["t_roof_us"], "frac": rf["frac"],
+                         "tensor_frac": rf["tensor_frac"], "hbm_frac": rf["hbm_frac"]},
+            "valid_slots": wl.num_valid, "launches_per_step": r["launches_per_step"],
+            "clocks": r["clocks"]}
 
 
 def run_reference(args):
@@ -465,6 +581,8 @@ def main():
                     help="seconds of oracle time for the cpu_baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload (skip the per_config block)")
     ap.add_argument("--kernel", default="decode", choices=["decode", "topk", "indexer", "select"],
                     help="decode: the attention path (the default line); topk: the top-k "
                          "selection with the page-table emit; indexer: the indexer scores; "
@@ -495,81 +613,30 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     smla.lib()
+    peaks, peak_kind = load_peaks()
+    flush = L2Flush(dev)
+    barrier = torch.distributed.barrier if ws > 1 else None
+
+    # ---- the other workloads first (one at a time, freed after), single-GPU runs only
+    per_config = None
+    if ws == 1 and not args.no_per_config:
+        per_config = {}
+        for name, cfg in workloads.CONFIGS.items():
+            if name == args.workload:
+                continue
+            wl_c = workloads.make(cfg, device=dev)
+            r = measure_decode(cfg, wl_c, dev, args.steps, args.warmup, flush, local)
+            per_config[name] = per_config_entry(cfg, wl_c, r, peaks)
+            del wl_c, r
+            torch.cuda.empty_cache()
+
     spec = workloads.CONFIGS[args.workload]
     wl = workloads.make(spec, device=dev)
-    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    op = smla.SparseMLADecode(spec.b, spec.s_q, spec.h_q, spec.topk, wl.kv.shape[0], device=dev,
-                              num_sms=num_sms)
-    out = torch.empty(spec.b, spec.s_q, spec.h_q, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(spec.b, spec.h_q, spec.s_q, dtype=torch.float32, device=dev)
-    flush = L2Flush(dev)
+    r = measure_decode(spec, wl, dev, args.steps, args.warmup, flush, local, barrier)
+    op, out, lse = r["op"], r["out"], r["lse"]
     stream = torch.cuda.current_stream(dev)
-    st = stream.cuda_stream
-    d = op.dims
-
-    def sched():
-        smla.sparse_mla_sched_meta(d, num_sms, op.sched.data_ptr(), op.sched_bytes, st)
-
-    def decode():
-        smla.sparse_mla_decode_fwd(d, num_sms, wl.q.data_ptr(), wl.kv.data_ptr(),
-                                   wl.indices.data_ptr(), wl.sm_scale, op.sched.data_ptr(),
-                                   op.workspace.data_ptr(), op.accum_bytes, out.data_ptr(),
-                                   lse.data_ptr(), st)
-
-    def combine():
-        smla.sparse_mla_combine(d, num_sms, op.sched.data_ptr(), op.workspace.data_ptr(),
-                                op.accum_bytes, out.data_ptr(), lse.data_ptr(), st)
-
-    launches_per_step = 3 if smla.sparse_mla_plan_has_splits(d, num_sms) else 2
-    # One step = plan + decode + combine, back to back on the stream (events only around the
-    # whole step, so the launches overlap as they do in use).
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        sched()
-        decode()
-        combine()
-        if ev is not None:
-            ev[1].record(stream)
-
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize(dev)
-    if op.device_status() != 0:
-        raise RuntimeError("device status word set during warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    dec_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        flush(k)
-        step(evs[k])
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - t0
-    # the decode kernel alone (for the roofline): events on the launching stream around it
-    for k in range(args.steps):
-        flush(k)
-        sched()
-        dec_evs[k][0].record(stream)
-        decode()
-        dec_evs[k][1].record(stream)
-        combine()
-    torch.cuda.synchronize(dev)
-    if ws > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    if op.device_status() != 0:
-        raise RuntimeError("device status word set during the timed steps")
-
-    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[0].elapsed_time(e[1]) for e in dec_evs]
+    step_ms, dec_ms, wall, clocks = r["step_ms"], r["dec_ms"], r["wall"], r["clocks"]
+    launches_per_step = r["launches_per_step"]
     t_step = sum(step_ms) / len(step_ms) / 1e3
     t_dec = sum(dec_ms) / len(dec_ms) / 1e3
     if ws > 1:
@@ -580,7 +647,6 @@ def main():
     nvalid = wl.num_valid
     alg_bytes = workloads.alg_bytes(wl)
     value = ws * flops / t_step / 1e12
-    peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / t_dec / 1e12
     traffic = traffic_from_profiles(os.path.join(CSRC, "decode_fwd.cu"),
@@ -592,7 +658,8 @@ def main():
     # of step k - 1 run on their own streams while step k computes (two device buffers of
     # each, events order the reuse).  Four index sets in rotation (each a shift of the
     # workload's positions by a multiple of 128 pages within every sequence, same mask) keep
-    # the rows a step gathers out of L2 from the steps before it (4 x 82 MB of rows > L2).
+    # the rows a step gathers out of L2 from the steps before it where the pool is larger
+    # than L2 (the prefill-shaped workload's 43 MB pool stays in L2 by design).
     q_h = wl.q.cpu().pin_memory()
     n_sets = 4
     i_sets = [s.pin_memory() for s in rotated_index_sets(wl.indices, wl.block_table,
@@ -678,12 +745,20 @@ def main():
             "kernel_ms": {"decode": statistics.mean(dec_ms),
                           "step_median": statistics.median(step_ms)},
             "wall_s_timed_region": wall,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"{peak_kind} bf16 burst",
-                         "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
-                         "alg_bytes_per_launch": alg_bytes,
-                         "hbm_frac_alg_bytes": alg_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"])},
+            "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak,
+                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                          "peak_kind": f"{peak_kind} bf16 burst",
+                          "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
+                          "alg_bytes_per_launch": alg_bytes,
+                          "hbm_frac_alg_bytes": alg_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"])}
+                         if roofline_of(wl, t_dec, peaks)["bound"] == "tensor" else
+                         {"bound": "hbm", "achieved": alg_bytes / t_dec / 1e9,
+                          "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                          "frac": alg_bytes / t_dec / 1e9 / float(peaks["hbm_gbs"]),
+                          "traffic": traffic, "peak_kind": f"{peak_kind} copy bandwidth",
+                          "alg_bytes_per_launch": alg_bytes, "tflops": achieved}),
+            "roofline_combined": roofline_of(wl, t_dec, peaks),
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": {"value": ws * flops / t_e2e / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
