@@ -381,34 +381,36 @@ out:
 }
 
 // ---------------------------------------------------------------------------------------
-// S-CTA MMA warp (one lane): S[buf] = Q K^T for every block (36 MMAs of K = 16).
+// S-CTA MMA warp: S[buf] = Q K^T for every block (36 MMAs of K = 16).  The whole warp runs
+// the loop (waits included) and one elected lane issues each MMA and commit.
 __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bool stall) {
   // test hook: a wait that nothing ends, so every role runs into its bounded wait
   if (stall) {
-    c.wait(B_NEVER, 0);
+    c.wait_warp(B_NEVER, 0);
     return;
   }
   uint32_t g = 0, item = 0;
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
-    if (!c.wait(B_Q_FULL, item & 1)) return;
+    if (!c.wait_warp(B_Q_FULL, item & 1)) return;
     for (int blk = pl.first_block(req); blk < pl.last_block(req); ++blk, ++g) {
       const uint32_t st = g & 1, sb = g % NSBUF;
-      if (!c.wait(B_KT_FULL + st, (g >> 1) & 1)) return;
-      if (g >= NSBUF && !c.wait(B_S_EMPTY + sb, ((g / NSBUF) - 1) & 1)) return;
+      if (!c.wait_warp(B_KT_FULL + st, (g >> 1) & 1)) return;
+      if (g >= NSBUF && !c.wait_warp(B_S_EMPTY + sb, ((g / NSBUF) - 1) & 1)) return;
       tc_fence_after();
       const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * KT_STAGE, 16, 1024, 2);
       const uint32_t d = tbase + TM_S + sb * BT;
 #pragma unroll 4  // kept rolled: the issuing warp shares its instruction cache with the others
       for (int kk = 0; kk < 36; ++kk)  // descriptor start addresses advance in 16-byte units
-        mma_ts(d, tbase + TM_Q + kk * 8, bdesc + ((((kk >> 2) * CHUNK) + (kk & 3) * 32) >> 4),
-               IDESC_QK, kk > 0);
-      mma_commit(c.bar(B_S_FULL + sb));
-      mma_commit(c.bar(B_KT_EMPTY + st));
+        mma_ts_warp(d, tbase + TM_Q + kk * 8,
+                    bdesc + ((((kk >> 2) * CHUNK) + (kk & 3) * 32) >> 4), IDESC_QK, kk > 0);
+      mma_commit_warp(c.bar(B_S_FULL + sb));
+      mma_commit_warp(c.bar(B_KT_EMPTY + st));
     }
   }
 }
 
-// O-CTA MMA warp (one lane): O += P V for every block (4 K-steps x 2 N-halves).
+// O-CTA MMA warp: O += P V for every block (4 K-steps x 2 N-halves); the whole warp runs the
+// loop and one elected lane issues.
 __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
   uint32_t g = 0, item = 0;
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
@@ -416,10 +418,10 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
     for (int blk = b0; blk < b1; ++blk, ++g) {
       const uint32_t st = g & 1, ms = g % NMSG, mpar = (g / NMSG) & 1;
       const bool first = blk == b0;
-      if (!c.wait(B_VT_FULL + st, (g >> 1) & 1)) return;
-      if (!c.wait(B_MSG_FULL + ms, mpar, true)) return;
-      if (!c.wait(B_CORR + ms, mpar)) return;
-      if (first && item >= 1 && !c.wait(B_O_EMPTY, (item - 1) & 1)) return;
+      if (!c.wait_warp(B_VT_FULL + st, (g >> 1) & 1)) return;
+      if (!c.wait_warp(B_MSG_FULL + ms, mpar, true)) return;
+      if (!c.wait_warp(B_CORR + ms, mpar)) return;
+      if (first && item >= 1 && !c.wait_warp(B_O_EMPTY, (item - 1) & 1)) return;
       tc_fence_after();
       const uint64_t adesc = umma_desc(c.sbase + OFF_MSG + ms * MSG_STRIDE, 16, 1024, 2);
       const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * VT_STAGE, CHUNK, 1024, 2);
@@ -427,13 +429,13 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
       for (int kk = 0; kk < BT / 16; ++kk) {
 #pragma unroll
         for (int nh = 0; nh < 2; ++nh)  // descriptor start addresses advance in 16-byte units
-          mma_ss(tbase + nh * 256, adesc + (kk * 32 >> 4),
-                 bdesc + ((nh * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV, !(first && kk == 0));
+          mma_ss_warp(tbase + nh * 256, adesc + (kk * 32 >> 4),
+                      bdesc + ((nh * 4 * CHUNK + kk * 2048) >> 4), IDESC_PV, !(first && kk == 0));
       }
-      mma_commit(c.bar(B_VT_EMPTY + st));
-      mma_commit(c.bar(B_PV_DONE + ms));
-      if (blk == b1 - 1) mma_commit(c.bar(B_O_FULL));
-      if (blk == b1 - 1 && req == pl.end_req) mma_commit(c.bar(B_LAST));
+      mma_commit_warp(c.bar(B_VT_EMPTY + st));
+      mma_commit_warp(c.bar(B_PV_DONE + ms));
+      if (blk == b1 - 1) mma_commit_warp(c.bar(B_O_FULL));
+      if (blk == b1 - 1 && req == pl.end_req) mma_commit_warp(c.bar(B_LAST));
     }
   }
 }
@@ -937,12 +939,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (scores) role_dequant<true, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
       else role_dequant<false, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
     } else if (warp == 12) {
-      if (lane == 0) {
-        if (scores) role_mma_scores(c, pl, tbase, p.test_stall != 0);
-        else role_mma_values(c, pl, tbase);
-        mma_commit(c.bar(B_DRAIN));  // every issued MMA has finished before TMEM is freed
-        c.drain(B_DRAIN, 0);
-      }
+      if (scores) role_mma_scores(c, pl, tbase, p.test_stall != 0);
+      else role_mma_values(c, pl, tbase);
+      mma_commit_warp(c.bar(B_DRAIN));  // every issued MMA has finished before TMEM is freed
+      if (lane == 0) c.drain(B_DRAIN, 0);
     } else if (warp == 8) {
       if (!scores && lane == 0) role_relay(c, pl);
     } else if (warp == 4) {

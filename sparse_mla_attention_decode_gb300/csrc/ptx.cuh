@@ -217,6 +217,34 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
       "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Warp-collective forms: every lane of a converged warp executes the instruction and
+// elect.sync lets exactly one of them issue it.  Issuing tcgen05 MMAs this way keeps the
+// issuing warp converged (operands uniform across the warp); MMAs issued from one lane of a
+// diverged warp issue far more slowly, and each shared-memory access of that lane between
+// them stalls the issue until the queued operand fetches drain.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
+
 // Arrive on a local mbarrier once all previously issued tcgen05 ops of this thread finish.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
