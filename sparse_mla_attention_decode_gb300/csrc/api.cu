@@ -69,7 +69,7 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
+smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts, int* sms_out = nullptr) {
   if (num_sms <= 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
@@ -79,6 +79,7 @@ smla_status resolve_parts(const smla_dims* d, int num_sms, int* parts) {
   const int sq = d->s_q > 0 ? d->s_q : 1;
   int p = num_sms / sq / 2;
   *parts = p < 1 ? 1 : p;
+  if (sms_out) *sms_out = num_sms;
   return SMLA_OK;
 }
 
@@ -245,8 +246,8 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
       !aligned(sched_meta, 16) || !aligned(indices, 4) || !aligned(lse, 4))
     return SMLA_ERR_ALIGNMENT;
   if ((st = check_opts(opts)) != SMLA_OK) return st;
-  int parts = 0;
-  if ((st = resolve_parts(dims, num_sms, &parts)) != SMLA_OK) return st;
+  int parts = 0, sms = 0;
+  if ((st = resolve_parts(dims, num_sms, &parts, &sms)) != SMLA_OK) return st;
   const AccumLayout A = workspace_layout(dims, parts);
   if (A.bytes > 0 && !workspace) return SMLA_ERR_INVALID_ARG;
   if (workspace_bytes < A.bytes) return SMLA_ERR_WORKSPACE;
@@ -291,6 +292,12 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.s_q = dims->s_q;
   p.h_q = dims->h_q;
   p.topk = dims->topk;
+  // one wave of 2-CTA clusters: with more query positions than clusters that fit (one
+  // partition each then), every cluster walks several positions in one launch
+  {
+    const int fit = sms / (2 * parts);
+    p.s_step = dims->s_q < fit ? dims->s_q : (fit < 1 ? 1 : fit);
+  }
   p.extra_kv = extra ? static_cast<const uint8_t*>(opts->extra_kv_cache) : nullptr;
   p.extra_indices = extra ? opts->extra_indices : nullptr;
   p.extra_topk_length = extra ? opts->extra_topk_length : nullptr;

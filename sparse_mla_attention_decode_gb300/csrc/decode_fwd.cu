@@ -163,22 +163,41 @@ struct Ctx {
 
 // The work of one partition: requests [begin_req, end_req], each with a block range, walked
 // block by block in the same order by every role of both CTAs.
+// A cluster's work: the request range of its partition (blocks [begin_block, nb) of
+// begin_req, whole requests, blocks [0, end_block) of end_req), for each query position
+// s = s0, s0 + s_step, ... below s_q in turn.  One (s, request) pair is an item; a cluster's
+// items follow one another through the same pipeline, their counters running on.
 struct Plan {
   int begin_req, end_req, begin_block, end_block, begin_split, nb;
+  int s0, s_step, s_q;
   __device__ int first_block(int req) const { return req == begin_req ? begin_block : 0; }
   __device__ int last_block(int req) const { return req == end_req ? end_block : nb; }
+  __device__ int last_s() const { return s0 + ((s_q - 1 - s0) / s_step) * s_step; }
+  __device__ bool last_item(int s, int req) const { return req == end_req && s + s_step >= s_q; }
+  __device__ int blocks_per_s() const {
+    int n = 0;
+    for (int r = begin_req; r <= end_req; ++r) n += last_block(r) - first_block(r);
+    return n;
+  }
 };
 struct Cursor {
-  int req, blk;  // current block; req > end_req once past the end
+  int s, req, blk;  // current block; s >= s_q once past the end
+  uint32_t item;    // items begun before the current one
   __device__ void start(const Plan& pl) {
+    s = pl.s0;
     req = pl.begin_req;
     blk = pl.first_block(req);
+    item = 0;
   }
-  __device__ bool done(const Plan& pl) const { return req > pl.end_req; }
+  __device__ bool done(const Plan& pl) const { return s >= pl.s_q; }
   __device__ void next(const Plan& pl) {
     if (++blk >= pl.last_block(req)) {
-      ++req;
-      if (req <= pl.end_req) blk = pl.first_block(req);
+      ++item;
+      if (++req > pl.end_req) {
+        req = pl.begin_req;
+        s += pl.s_step;
+      }
+      blk = pl.first_block(req);
     }
   }
 };
@@ -295,7 +314,7 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
 // kExtra: the kernel instance with an extra cache, whose blocks follow the main list's in the
 // plan (blocks nb_main and up read the extra indices and rows).
 template <bool kScores, bool kLen, bool kExtra>
-__device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int s, int t) {
+__device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int t) {
   using RC = RowCopy<kScores>;
   const int w = t >> 5, lane = t & 31;  // warp w of the 8 dequant warps
   const int j = lane & 7, rsel = lane >> 3;
@@ -308,8 +327,8 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
   // Lane r < 8 holds the index of row w + 8 r of a block.
   auto idx_of = [&](const Cursor& k) -> int32_t {
     if (lane >= 8 || k.done(pl)) return -1;
-    if (in_extra(k)) return load_extra_index(p, s, k.req, k.blk - p.nb_main, w + 8 * lane);
-    return load_index<kLen>(p, s, k.req, k.blk, w + 8 * lane);
+    if (in_extra(k)) return load_extra_index(p, k.s, k.req, k.blk - p.nb_main, w + 8 * lane);
+    return load_index<kLen>(p, k.s, k.req, k.blk, w + 8 * lane);
   };
   auto valid_bits = [&](int32_t ix, bool extra) -> uint32_t {
     const int rows = extra ? p.extra_rows : p.num_rows;
@@ -343,8 +362,7 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
     // each token's Q passes through the key-tile region on its way to tensor memory: the
     // first tile of a request waits until it has been read out
-    if (kScores && cur.blk == pl.first_block(cur.req) &&
-        !c.wait_warp(B_QREAD, static_cast<uint32_t>(cur.req - pl.begin_req) & 1u))
+    if (kScores && cur.blk == pl.first_block(cur.req) && !c.wait_warp(B_QREAD, cur.item & 1u))
       goto out;
     {
       const uint32_t tile = c.sbase + OFF_TILE + st * stage_bytes;
@@ -390,6 +408,7 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bo
     return;
   }
   uint32_t g = 0, item = 0;
+  for (int s = pl.s0; s < pl.s_q; s += pl.s_step)
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     if (!c.wait_warp(B_Q_FULL, item & 1)) return;
     for (int blk = pl.first_block(req); blk < pl.last_block(req); ++blk, ++g) {
@@ -413,6 +432,7 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bo
 // loop and one elected lane issues.
 __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
   uint32_t g = 0, item = 0;
+  for (int s = pl.s0; s < pl.s_q; s += pl.s_step)
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     for (int blk = b0; blk < b1; ++blk, ++g) {
@@ -435,7 +455,7 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
       mma_commit_warp(c.bar(B_VT_EMPTY + st));
       mma_commit_warp(c.bar(B_PV_DONE + ms));
       if (blk == b1 - 1) mma_commit_warp(c.bar(B_O_FULL));
-      if (blk == b1 - 1 && req == pl.end_req) mma_commit_warp(c.bar(B_LAST));
+      if (blk == b1 - 1 && pl.last_item(s, req)) mma_commit_warp(c.bar(B_LAST));
     }
   }
 }
@@ -498,7 +518,7 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
 }
 
 // S-CTA softmax warpgroup: thread i owns head row i (tensor-memory lane i).
-__device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl, int s,
+__device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl,
                              uint32_t tbase, int i) {
   const uint32_t lane_base = static_cast<uint32_t>((i >> 5) * 32) << 16;
   const uint32_t tq = tbase + lane_base + TM_Q;
@@ -507,9 +527,10 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   const uint32_t peer_full = mapa(c.bar(B_MSG_FULL), 1);
   const bool live = i < p.h_q;
   uint32_t qbad = 0;
-  uint32_t g = 0;
-  if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + s, i, qbad, 0)) goto out;
-  for (int req = pl.begin_req; req <= pl.end_req; ++req) {
+  uint32_t g = 0, item = 0;
+  if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + pl.s0, i, qbad, 0)) goto out;
+  for (int s = pl.s0; s < p.s_q; s += pl.s_step)
+  for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     float m = -INFINITY;  // running max (base-2 units) used as the exponent reference
     float l = 0.f;        // running exp-sum against m
@@ -597,11 +618,13 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
         bulk_s2s_cluster(peer_msg + st * MSG_STRIDE, msg, MSG_BYTES, peer_full + st * 8);
       }
     }
-    // every QK^T of this range has completed: stage the next query token's Q
-    if (req < pl.end_req &&
-        !stage_q_bulk(p, c, tq, (req + 1) * p.s_q + s, i, qbad,
-                      static_cast<uint32_t>(req + 1 - pl.begin_req)))
-      goto out;
+    // every QK^T of this range has completed: stage the next item's Q (the next request at
+    // this position, else the first request at the cluster's next position)
+    if (!pl.last_item(s, req)) {
+      const int nreq = req < pl.end_req ? req + 1 : pl.begin_req;
+      const int ns = req < pl.end_req ? s : s + pl.s_step;
+      if (!stage_q_bulk(p, c, tq, nreq * p.s_q + ns, i, qbad, item + 1)) goto out;
+    }
   }
 out:
   if (qbad) atomicOr(c.status, SMLA_DEV_Q_RANGE);
@@ -740,8 +763,8 @@ __device__ bool drain_o_tma(const DecodeParams& p, const Ctx& c, uint32_t to, in
 // O-CTA store issuer (one lane of an otherwise idle warp): for the partition's last range,
 // sends each staged output box with a tiled TMA store as soon as all its rows are in, and
 // waits for the stores before the CTA may leave.
-__device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Plan& pl, int s) {
-  const int req = pl.end_req;
+__device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Plan& pl) {
+  const int req = pl.end_req, s = pl.last_s();
   const int first_slot = p.nsplits[req];
   const bool no_split = p.nsplits[req + 1] - first_slot == 1;
   const int split = req == pl.begin_req ? pl.begin_split : first_slot;
@@ -772,11 +795,12 @@ __device__ void role_store_issuer(const DecodeParams& p, const Ctx& c, const Pla
 
 // ---------------------------------------------------------------------------------------
 // O-CTA correction + epilogue warpgroup: thread i owns O row i.
-__device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const Plan& pl, int s,
+__device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const Plan& pl,
                                      uint32_t tbase, int i) {
   const uint32_t to = tbase + (static_cast<uint32_t>((i >> 5) * 32) << 16);
   const bool live = i < p.h_q;
   uint32_t g = 0, item = 0;
+  for (int s = pl.s0; s < p.s_q; s += pl.s_step)
   for (int req = pl.begin_req; req <= pl.end_req; ++req, ++item) {
     const int b0 = pl.first_block(req), b1 = pl.last_block(req);
     float invl = 0.f;
@@ -812,7 +836,7 @@ __device__ void role_values_epilogue(const DecodeParams& p, const Ctx& c, const 
     const bool no_split = p.nsplits[req + 1] - first_slot == 1;
     const int split = req == pl.begin_req ? pl.begin_split : first_slot;
     const int tok = req * p.s_q + s;
-    if (req == pl.end_req) {  // the value tiles are free now: stage O there for TMA stores
+    if (pl.last_item(s, req)) {  // the value tiles are free now: stage O there for TMA stores
       // bf16 rows: this warpgroup takes columns 0-255, warps 8-11 take 256-511
       const bool bf16_rows = no_split || p.partials_bf16;
       if (!drain_o_tma(p, c, to, i, bf16_rows, invl, 0, bf16_rows ? 8 : 16)) return;
@@ -832,8 +856,8 @@ __device__ void drain_o_second_half(const DecodeParams& p, const Ctx& c, const P
                                     uint32_t tbase, int row) {
   const int req = pl.end_req;
   if (!(p.nsplits[req + 1] - p.nsplits[req] == 1 || p.partials_bf16)) return;
-  uint32_t nblk = 0;
-  for (int r = pl.begin_req; r <= pl.end_req; ++r) nblk += pl.last_block(r) - pl.first_block(r);
+  const uint32_t nblk = static_cast<uint32_t>(pl.blocks_per_s()) *
+                        static_cast<uint32_t>((pl.s_q - 1 - pl.s0) / pl.s_step + 1);
   const uint32_t msg = c.sbase + OFF_MSG + ((nblk - 1) % NMSG) * MSG_STRIDE;
   if (!c.wait_warp(B_LAST, 0)) return;
   tc_fence_after();
@@ -847,6 +871,7 @@ __device__ void drain_o_second_half(const DecodeParams& p, const Ctx& c, const P
 __device__ void role_relay(const Ctx& c, const Plan& pl) {
   const uint32_t peer_free = mapa(c.bar(B_MSG_FREE), 0);
   uint32_t g = 0;
+  for (int s = pl.s0; s < pl.s_q; s += pl.s_step)
   for (int req = pl.begin_req; req <= pl.end_req; ++req)
     for (int blk = pl.first_block(req); blk < pl.last_block(req); ++blk, ++g) {
       const uint32_t st = g % NMSG;
@@ -866,7 +891,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool scores = rank == 0;
-  const int part = blockIdx.x >> 1, s = blockIdx.y;
+  const int part = blockIdx.x >> 1;
   Ctx c;
   c.sbase = smem_u32(sm);
   c.abort_flag = reinterpret_cast<volatile uint32_t*>(sm + OFF_ABORT);
@@ -927,17 +952,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   pl.end_block = m[3];
   pl.begin_split = m[4];
   pl.nb = p.nb_total;
+  pl.s0 = static_cast<int>(blockIdx.y);
+  pl.s_step = p.s_step;
+  pl.s_q = p.s_q;
   const bool active = pl.begin_req < p.b;
 
   if (active) {
     const int dq = dequant_index(warp);
     c.role = (scores ? 0u : 8u) + (warp < 4 ? 1u : dq >= 0 ? 2u : warp == 12 ? 3u : 4u);
     if (warp < 4) {
-      if (scores) role_softmax(p, c, pl, s, tbase, threadIdx.x);
-      else role_values_epilogue(p, c, pl, s, tbase, threadIdx.x);
+      if (scores) role_softmax(p, c, pl, tbase, threadIdx.x);
+      else role_values_epilogue(p, c, pl, tbase, threadIdx.x);
     } else if (dq >= 0) {
-      if (scores) role_dequant<true, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
-      else role_dequant<false, kLen, kExtra>(p, c, pl, s, dq * 32 + lane);
+      if (scores) role_dequant<true, kLen, kExtra>(p, c, pl, dq * 32 + lane);
+      else role_dequant<false, kLen, kExtra>(p, c, pl, dq * 32 + lane);
     } else if (warp == 12) {
       if (scores) role_mma_scores(c, pl, tbase, p.test_stall != 0);
       else role_mma_values(c, pl, tbase);
@@ -946,7 +974,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     } else if (warp == 8) {
       if (!scores && lane == 0) role_relay(c, pl);
     } else if (warp == 4) {
-      if (!scores && lane == 0) role_store_issuer(p, c, pl, s);
+      if (!scores && lane == 0) role_store_issuer(p, c, pl);
     }
     __syncwarp();
     if (!scores && warp >= 8 && warp < 12) drain_o_second_half(p, c, pl, tbase, (warp & 3) * 32 + lane);
@@ -972,7 +1000,7 @@ cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream)
   // Programmatic stream serialisation: the kernel's set-up may overlap the preceding kernel;
   // griddepcontrol.wait inside holds every read of the plan and the inputs until it is done.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * parts), static_cast<unsigned>(p.s_q), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * parts), static_cast<unsigned>(p.s_step), 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;

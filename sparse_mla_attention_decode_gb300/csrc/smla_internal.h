@@ -75,6 +75,8 @@ struct DecodeParams {
   int extra_topk, extra_rows;
   int nb_main, nb_total;    // blocks of the main list; of both lists (the plan's blocks)
   int b, s_q, h_q, topk;
+  // clusters per partition: cluster y takes the query positions s = y, y + s_step, ... (< s_q)
+  int s_step;
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
   int store32;              // out and the workspace are 32-byte aligned (256-bit stores)
