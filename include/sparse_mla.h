@@ -65,6 +65,13 @@ typedef enum {
 #define SMLA_DEV_Q_RANGE 0x2u       /* |q| above 65504: not representable in the fp16 MMA */
 #define SMLA_DEV_SCALE_RANGE 0x4u   /* a KV scale * 256 outside the fp16 normal range */
 #define SMLA_DEV_TOPK_TABLE 0x8u    /* top-k: a selected position lies beyond the page table */
+#define SMLA_DEV_NAN_INPUT 0x10u    /* a valid slot scored NaN or +inf: a NaN e4m3 code, scale or
+                                       bf16 value (or bf16 +inf) in its row or in q, as the
+                                       definition has it (every head of the token, or the heads
+                                       scoring +inf, get out = NaN and lse = NaN), or a key
+                                       value with |code * scale| * 256 above 65504, beyond the
+                                       fp16 MMA's range (those heads are NaN; the definition's
+                                       value is finite) */
 
 /* Problem sizes.  Only d_qk = 576, d_v = 512, page_block_size = 64, h_q in {64, 128} are
  * supported ("FlashMLA 与 DSA", section 3.1: the 656-byte V3.2 row; section 6.1: h_q 64/128,

@@ -38,6 +38,7 @@ SMLA_OK = 0
 SMLA_ERR_WORKSPACE = 4
 SMLA_ERR_TIMEOUT = 6
 SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE, SMLA_DEV_TOPK_TABLE = 0x1, 0x2, 0x4, 0x8
+SMLA_DEV_NAN_INPUT = 0x10
 SMLA_SCORES_BF16, SMLA_SCORES_FP32 = 0, 1
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",

@@ -85,7 +85,12 @@ enum Bar {
 constexpr int OFF_BARS = OFF_MISC;
 constexpr int OFF_TMEM_SLOT = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 16;
-constexpr int SMEM_BYTES = OFF_ABORT + 16 + 1024;  // + alignment slack
+// S-CTA slot validity of a key-tile stage, on its way to tensor memory: 32 identical rows of
+// 16 bytes, of which bytes 0-7 hold the block's bits (byte w: dequant warp w's rows w + 8 r,
+// bit r)
+constexpr int OFF_VMASK = (OFF_ABORT + 16 + 127) & ~127;
+constexpr int VMASK_STAGE = 32 * 16;
+constexpr int SMEM_BYTES = OFF_VMASK + NSTAGE * VMASK_STAGE + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // warps: 0-3 softmax (S) / correction + epilogue (O); 5-7, 9-11, 13-14 gather + dequant;
@@ -97,7 +102,12 @@ __device__ __forceinline__ int dequant_index(int warp) {
   if ((warp & 3) == 0 || warp < 5 || warp > 14) return -1;
   return warp - 5 - ((warp - 4) >> 2);  // 5, 6, 7 -> 0, 1, 2; 9, 10, 11 -> 3, 4, 5; 13, 14 -> 6, 7
 }
-constexpr uint32_t TM_Q = 0, TM_S = 288;  // S-CTA columns; the O-CTA uses all 512 for O
+// S-CTA tensor-memory columns: Q (fp16, 288), three score buffers (3 x 64) and the slot
+// validity of the last NVMASK blocks (4 columns each, every lane the same); the O-CTA uses
+// all 512 for O
+constexpr uint32_t TM_Q = 0, TM_S = 288, TM_M = 480;
+constexpr int NVMASK = 8;
+static_assert(TM_S + NSBUF * BT == TM_M && TM_M + 4 * NVMASK == 512, "tensor-memory columns");
 constexpr uint32_t IDESC_QK = umma_idesc_f16(128, BT, 0);
 constexpr uint32_t IDESC_PV = umma_idesc_f16(128, 256, 1);
 constexpr uint64_t kWaitNs = 1000000000ull;  // a wait gives up after one second
@@ -385,6 +395,10 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
         store_rows<kScores>(tile, w + 8 * r, j, (vmask >> r) & 1u, nope, scales, rope, bad);
       }
     }
+    // the block's validity bits for the softmax (this warp's byte of all 32 rows); the MMA
+    // warp copies them into tensor memory with the tile's QK.  The stage is free: its last
+    // copy was done with the QK of block g - 2.
+    if (kScores) st_shared_u8(c.sbase + OFF_VMASK + st * VMASK_STAGE + lane * 16 + w, vmask & 0xFFu);
     fence_proxy_async_smem();
     mbar_arrive(c.bar(bfull + st));
     vmask >>= 8;
@@ -416,6 +430,10 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bo
       if (!c.wait_warp(B_KT_FULL + st, (g >> 1) & 1)) return;
       if (g >= NSBUF && !c.wait_warp(B_S_EMPTY + sb, ((g / NSBUF) - 1) & 1)) return;
       tc_fence_after();
+      // the block's validity bits into columns TM_M + 4 (g % NVMASK); the softmax of block
+      // g - 8, which read them last, released its scores before the QK of block g - 5
+      tmem_cp_32x128b_x4_warp(tbase + TM_M + 4 * (g % NVMASK),
+                              umma_desc(c.sbase + OFF_VMASK + st * VMASK_STAGE, 16, 128, 0));
       const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * KT_STAGE, 16, 1024, 2);
       const uint32_t d = tbase + TM_S + sb * BT;
 #pragma unroll 4  // kept rolled: the issuing warp shares its instruction cache with the others
@@ -517,7 +535,48 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
   return true;
 }
 
-// S-CTA softmax warpgroup: thread i owns head row i (tensor-memory lane i).
+// p = 2^(s * c2 - mref) for the 64 scores of row i (tensor-memory columns [scol, scol + 64)),
+// stored as fp16 into the row's message slot; returns their sum.  kMasked: slot k is valid
+// when bit 8 (k % 8) + k / 8 of vmask is set (byte w: rows w + 8 r of the dequant warp w);
+// invalid slots get p = 0 (their keys are NaN).  The scores are read from tensor memory 32 at
+// a time and the loop stays rolled (a small hot loop next to the other roles' code).
+template <bool kMasked>
+__device__ __forceinline__ float exp_pass(uint32_t scol, uint32_t msg, int i, float c2, float mref,
+                                          uint64_t vmask) {
+  float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t r32[32];
+    tmem_ld16(scol + hh * 32, r32);
+    tmem_ld16(scol + hh * 32 + 16, r32 + 16);
+    const uint64_t vh = vmask >> (4 * hh);  // slot 32 hh + j: bit 8 (j % 8) + j / 8
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k0 = 8 * k + 2 * e;
+        float p0 = ex2(fmaf(__uint_as_float(r32[k0]), c2, -mref));
+        float p1 = ex2(fmaf(__uint_as_float(r32[k0 + 1]), c2, -mref));
+        if (kMasked) {
+          p0 = (vh >> (8 * (k0 & 7) + (k0 >> 3))) & 1u ? p0 : 0.f;
+          p1 = (vh >> (8 * ((k0 + 1) & 7) + ((k0 + 1) >> 3))) & 1u ? p1 : 0.f;
+        }
+        sq[e] += p0 + p1;
+        w[e] = pack_f16x2(p0, p1);
+      }
+      st_shared_v4(msg + sw128_chunk(i, 4 * hh + k), w[0], w[1], w[2], w[3]);
+    }
+  }
+  return (sq[0] + sq[1]) + (sq[2] + sq[3]);
+}
+
+// S-CTA softmax warpgroup: thread i owns head row i (tensor-memory lane i).  The exponentials
+// of invalid slots are zeroed by the block's validity bits (from the dequant warps, through
+// tensor memory), so a NaN
+// or +inf score of a valid slot (a NaN code in its row) is not masked: it makes the row's sum
+// NaN, hence O and lse, as the definition gives, and the status word gets SMLA_DEV_NAN_INPUT.
 __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl,
                              uint32_t tbase, int i) {
   const uint32_t lane_base = static_cast<uint32_t>((i >> 5) * 32) << 16;
@@ -526,7 +585,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   const uint32_t peer_msg = mapa(c.sbase + OFF_MSG, 1);
   const uint32_t peer_full = mapa(c.bar(B_MSG_FULL), 1);
   const bool live = i < p.h_q;
-  uint32_t qbad = 0;
+  uint32_t qbad = 0, nan_row = 0;
   uint32_t g = 0, item = 0;
   if (!stage_q_bulk(p, c, tq, pl.begin_req * p.s_q + pl.s0, i, qbad, 0)) goto out;
   for (int s = pl.s0; s < p.s_q; s += pl.s_step)
@@ -538,17 +597,25 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       const uint32_t sb = g % NSBUF, st = g % NMSG;
       if (!c.wait_warp(B_S_FULL + sb, (g / NSBUF) & 1)) goto out;
       tc_fence_after();
-      uint32_t sr[BT];
-#pragma unroll
-      for (int k = 0; k < BT / 16; ++k) tmem_ld16(ts + sb * BT + k * 16, sr + k * 16);
-      tmem_wait_ld();
+      // the block's validity bits, copied into tensor memory with its QK (the same commit)
+      uint32_t mk[2];
+      tmem_ld2(tbase + lane_base + TM_M + 4 * (g % NVMASK), mk);
       // block max in base-2 units: fmaxf skips the NaN scores of invalid slots, and the scale
-      // is positive, so it applies to the max of the raw scores (four chains for ILP)
+      // is positive, so it applies to the max of the raw scores (four chains for ILP; two
+      // halves of 32 scores, so that few registers are live)
       const float c2 = p.score_scale_log2;
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < BT; ++k) mq[k & 3] = fmaxf(mq[k & 3], __uint_as_float(sr[k]));
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[32];
+        tmem_ld16(ts + sb * BT + hh * 32, sr);
+        tmem_ld16(ts + sb * BT + hh * 32 + 16, sr + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mq[k & 3] = fmaxf(mq[k & 3], __uint_as_float(sr[k]));
+      }
       const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c2;
+      const uint64_t vmask = (static_cast<uint64_t>(mk[1]) << 32) | mk[0];
       // lazy rescale: the reference only moves when a block's max passes it by more than 8
       // (p then stays <= 256, which fp16 holds with full precision)
       float alpha = 1.f;
@@ -562,32 +629,14 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       // the message slot is free again once the O-CTA's PV that read it has finished
       if (g >= NMSG && !c.wait_warp(B_MSG_FREE + st, ((g / NMSG) - 1) & 1, true)) goto out;
       const uint32_t msg = c.sbase + OFF_MSG + st * MSG_STRIDE;
-      // p = 2^(s * c2 - mref); an invalid slot's NaN stays NaN through ex2 and fmaxf(NaN, 0)
-      // turns it into p = 0.  The scores are read again from tensor memory, 32 at a time, so
-      // this loop stays rolled (a small hot loop next to the other roles' code).
-      float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r32[32];
-        tmem_ld16(ts + sb * BT + hh * 32, r32);
-        tmem_ld16(ts + sb * BT + hh * 32 + 16, r32 + 16);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fmaxf(ex2(fmaf(__uint_as_float(r32[8 * k + 2 * e]), c2, -mref)), 0.f);
-            const float p1 = fmaxf(ex2(fmaf(__uint_as_float(r32[8 * k + 2 * e + 1]), c2, -mref)), 0.f);
-            sq[e] += p0 + p1;
-            w[e] = pack_f16x2(p0, p1);
-          }
-          st_shared_v4(msg + sw128_chunk(i, 4 * hh + k), w[0], w[1], w[2], w[3]);
-        }
-      }
+      // p = 2^(s * c2 - mref), 0 for an invalid slot (whose key is NaN).
+      // A block whose slots are all valid (the mask is the same for every row, so the branch
+      // is uniform) takes the loop without the mask.
+      const float sum = vmask == ~0ull
+                            ? exp_pass<false>(ts + sb * BT, msg, i, c2, mref, 0ull)
+                            : exp_pass<true>(ts + sb * BT, msg, i, c2, mref, vmask);
       tc_fence_before();
       mbar_arrive(c.bar(B_S_EMPTY + sb));  // every read of this score buffer is done
-      const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
       l = l * alpha + sum;
       st_shared_f32(msg + MSG_ALPHA + 4 * i, alpha);
       if (blk == b1 - 1) {
@@ -600,6 +649,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
         if (no_split && live && p.attn_sink != nullptr && l != 0.f)
           denom += ex2(fmaf(__ldg(p.attn_sink + i), 1.4426950408889634f, -m));
         st_shared_f32(msg + MSG_INVL + 4 * i, l == 0.f ? 0.f : 1.f / (denom * 256.f));
+        nan_row |= live && l != l;
         if (live) {
           if (no_split) {
             p.lse[(static_cast<size_t>(req) * p.h_q + i) * p.s_q + s] =
@@ -628,6 +678,7 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
   }
 out:
   if (qbad) atomicOr(c.status, SMLA_DEV_Q_RANGE);
+  if (nan_row) atomicOr(c.status, SMLA_DEV_NAN_INPUT);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -266,11 +266,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
   const size_t row_stride = static_cast<size_t>(p.s_q) * p.h_q;
   const float* lse2 = p.lse_accum + (static_cast<size_t>(first) * p.s_q + s) * p.h_q + h;
   float mx = -INFINITY;
-  for (int j = lane; j < n; j += 32) mx = fmaxf(mx, lse2[j * row_stride]);
+  bool nan = false;
+  for (int j = lane; j < n; j += 32) {
+    const float v = lse2[j * row_stride];
+    mx = fmaxf(mx, v);
+    nan |= v != v;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   __nv_bfloat16* out = p.out + ((static_cast<size_t>(req) * p.s_q + s) * p.h_q + h) * kDV;
   float* lse_out = p.lse + (static_cast<size_t>(req) * p.h_q + h) * p.s_q + s;
+  if (__any_sync(0xffffffffu, nan)) {  // a split saw a NaN or +inf score: the row is NaN
+    const uint32_t qnan = 0x7FC07FC0u;  // bf16 NaN pair
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint2*>(out + c * 128 + lane * 4) = make_uint2(qnan, qnan);
+    if (lane == 0) *lse_out = __uint_as_float(0x7FC00000u);
+    return;
+  }
   if (mx == -INFINITY) {  // every split empty: the defined output of a row with no valid slot
 #pragma unroll
     for (int c = 0; c < 4; ++c)

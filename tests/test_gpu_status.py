@@ -1,7 +1,7 @@
 """The device status word reports inputs outside the fp16 range the kernel computes in: a query
 value that would overflow fp16 (from the first and from a later request of a partition), and
 a KV scale whose product with 256 leaves the fp16 normal range.  Clean inputs give 0; the
-largest finite case does not trip the check.  (Valid inputs only: nothing here can fault.)"""
+largest scale in range does not trip the scale check.  (Valid inputs only: nothing here can fault.)"""
 
 import pytest
 import torch
@@ -57,7 +57,13 @@ def test_scale_range_flag(dev):
         flat = wl.kv.view(-1, 656)
         flat[row, 512 + 4:512 + 8] = torch.tensor([scale], dtype=torch.float32).view(torch.uint8).to(dev)
         assert _status(wl, 8) & smla.SMLA_DEV_SCALE_RANGE, scale
+    # the largest scale the fp16 path takes (255 * 256 = 65280) is not a scale-range error;
+    # with large codes in that group the products themselves overflow fp16, which the
+    # non-finite-score bit reports instead
     wl.kv = kv0.clone()
     flat = wl.kv.view(-1, 656)
     flat[row, 512:516] = torch.tensor([255.0], dtype=torch.float32).view(torch.uint8).to(dev)
+    assert not _status(wl, 8) & smla.SMLA_DEV_SCALE_RANGE
+    # and with codes small enough (|code| <= 1) the key stays finite: the word is clean
+    flat[row, 0:128] = torch.tensor([0x38, 0xB8], dtype=torch.uint8, device=dev).repeat(64)
     assert _status(wl, 8) == 0

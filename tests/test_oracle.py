@@ -236,6 +236,42 @@ def test_all_masked_row_defined_output():
     assert np.all(np.isfinite(lse[0]))
 
 
+def test_non_finite_key_values_follow_the_definition():
+    # the plain definition in exact arithmetic: a NaN anywhere in a valid key row makes every
+    # score of that token NaN, hence its whole output and lse; a +inf score gives inf - inf =
+    # NaN in the softmax; a -inf score only adds exp(-inf) = 0, the same as masking the slot
+    wl, q, kv, idx = _tiny(b=2, s_q=1, h=4, topk=8, seed=5)
+    out0, lse0 = oracle.sparse_mla_decode_full(q, kv, idx, wl.sm_scale)
+    flat = kv.reshape(-1, 656)
+    r = int(idx[0, 0, 3])
+    assert r not in set(idx[1, 0].tolist())
+    for where, patch in (("nope", {17: 0x7F}), ("rope", {528 + 2 * 5: 0xC0, 529 + 2 * 5: 0x7F})):
+        kv2 = kv.copy()
+        f2 = kv2.reshape(-1, 656)
+        for byte, v in patch.items():
+            f2[r, byte] = v
+        out, lse = oracle.sparse_mla_decode_full(q, kv2, idx, wl.sm_scale)
+        assert np.all(np.isnan(out[0])) and np.all(np.isnan(lse[0])), where
+        assert np.array_equal(out[1], out0[1]) and np.array_equal(lse[1], lse0[1]), where
+    # bf16 +inf in RoPE dim 5: heads whose q there is positive see +inf (NaN row), heads
+    # with a negative value see -inf (the slot drops out, as if it were masked)
+    kv3 = kv.copy()
+    f3 = kv3.reshape(-1, 656)
+    f3[r, 528 + 10], f3[r, 529 + 10] = 0x80, 0x7F
+    out, lse = oracle.sparse_mla_decode_full(q, kv3, idx, wl.sm_scale)
+    masked = idx.copy()
+    masked[0, 0, 3] = -1
+    om, lm = oracle.sparse_mla_decode_full(q, kv, masked, wl.sm_scale)
+    qr = oracle.bf16_decode(q[0, 0, :, 512 + 5])
+    assert np.all(qr != 0)
+    for h in range(4):
+        if qr[h] > 0:
+            assert np.all(np.isnan(out[0, 0, h])) and np.isnan(lse[0, h, 0])
+        else:
+            assert _rel(out[0, 0, h], om[0, 0, h]) < 1e-12 and abs(lse[0, h, 0] - lm[0, h, 0]) < 1e-12
+    assert (qr > 0).any() and (qr < 0).any()
+
+
 # --------------------------------------------------------------------------- splits / combine
 
 def test_combine_worked_example_corrected():
