@@ -102,6 +102,22 @@ def traffic_from_profiles(kernel_src: str, profile: str, alg_bytes=None):
     return traffic
 
 
+def traffic_from_pair_profile(sources, profile: str):
+    """DRAM bytes per step of a chain of kernels from one committed ncu summary that lists a
+    ``code_sha256 <file>: <hash>`` line per kernel source and their summed
+    ``dram_bytes_per_step``; None when the summary is missing or any source has changed."""
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    txt = open(path, encoding="utf-8").read()
+    for src in sources:
+        m = re.search(r"code_sha256 %s:\s*([0-9a-f]{64})" % re.escape(os.path.basename(src)), txt)
+        if not m or m.group(1) != code_sha256(src):
+            return None
+    m_b = re.search(r"dram_bytes_per_step:\s*([0-9.eE+]+)", txt)
+    return float(m_b.group(1)) if m_b else None
+
+
 def rotated_index_sets(indices, block_table, num_blocks: int, n_sets: int, shift_pages: int = 128):
     """n_sets index tensors (int32, host): the given one, then the same slots with every valid
     position of a sequence moved by j * shift_pages pages (cyclically within the sequence's
@@ -554,6 +570,10 @@ def run_select(args):
     clocks = sampler.stop()
     t = sum(ts) / len(ts)
     alg = b * pages * 8448 + b * (64 * 128 + 64 * 4) + b * k * 4
+    # both kernels of a step (the scores between them stay in L2 by design)
+    traffic = traffic_from_pair_profile(
+        [os.path.join(CSRC, "indexer.cu"), os.path.join(CSRC, "topk.cu")],
+        f"select_kernels_decode_b{b}_ctx{ctx}_k{k}.md")
     peaks, peak_src = load_peaks()
     peak = float(peaks["hbm_gbs"])
     achieved = alg / t / 1e9
@@ -565,7 +585,7 @@ def run_select(args):
         "config": {"workload": f"select_decode_b{b}_ctx{ctx}_k{k}", "requests": b, "ctx": ctx,
                    "topk": k, "scratch_bytes": scratch.numel(), "l2": FLUSH_NOTE},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{peak_src} copy bandwidth", "alg_bytes_per_launch": alg},
         "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
 

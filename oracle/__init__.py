@@ -11,6 +11,8 @@ code, header, table or constant.
 * ``combine.py`` -- the LSE-weighted merge of split partials.
 * ``online.py`` -- the base-2 online softmax recurrence, step by step.
 * ``variants.py`` -- per-token top-k length masking and the attention-sink output factor.
+* ``formats.py`` -- the later cache formats (V4, V4.1, FP4 extra: structure-of-arrays pages,
+  e8m0 / e4m3 group scales, d_qk = d_v = 512) decoded and attended in numpy.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle*.py`` (worked-example values from the pages, closed forms, brute force

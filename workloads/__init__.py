@@ -16,6 +16,15 @@ ue8m0-style scales; ``code = rn_e4m3(x / scale)`` with the quotient in fp32, sat
 Indices are physical token ids ``page * 64 + offset`` reached through a per-sequence page
 table whose pages are scattered at random over a shared pool.
 
+Later formats ("FlashMLA 与 DSA", sections 3.1 and 6.4; d_qk = 512): a page of 64 tokens holds
+the 64 data rows, then the 64 scale rows.  V4: 448 e4m3 NoPE codes + 64 bf16 RoPE values, then
+7 e8m0 scales (per 64 NoPE dims) + 1 zero pad byte (584 bytes a token).  V4.1: 512 e4m3 codes,
+then 16 e8m0 scales (per 32 dims) (528).  FP4 (extra cache only): 512 e2m1 values, two per
+byte with the even element in the low nibble, then 32 e4m3 scales (per 16 dims) (288).
+Quantisers: e8m0 scale = the power of two 2^ceil(log2(amax / 448)) (1 for an all-zero group),
+code = rn_e4m3(x / scale); FP4 scale = rn_e4m3(amax / 6) (1 for an all-zero group), code =
+the nearest e2m1 value of x / scale (ties to the even code, saturating at 6).
+
 The five benchmark workloads (``CONFIGS``) follow the configuration list this project is
 measured on; ``seed`` is the config's position 0..4.
 """
@@ -48,6 +57,11 @@ class Spec:
     sort_indices: bool = False  # sort each row ascending by physical id
     extra_pool_pages: int = 0
     seed: int = 0
+    kv_format: str = "v32"  # "v32" (656-byte rows, d_qk 576), "v4" or "v41" (d_qk 512)
+
+    @property
+    def d_qk(self) -> int:
+        return D_QK if self.kv_format == "v32" else 512
 
     @property
     def pages_per_seq(self) -> int:
@@ -122,6 +136,73 @@ def quantize_rows(x: torch.Tensor, ue8m0: bool = False) -> torch.Tensor:
     return out
 
 
+# bytes of one token's data row and scale row in the later formats
+FMT_BYTES = {"v4": (448 + 2 * D_ROPE, 8), "v41": (512, 16), "v41_fp4": (256, 32)}
+
+
+def _e8m0_codes(amax: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """(scale fp32, e8m0 byte) per group: the power of two 2^ceil(log2(amax / 448))."""
+    scale = ue8m0_scale(amax / E4M3_MAX)
+    scale = torch.where(amax == 0, torch.ones_like(scale), scale).float()
+    code = ((scale.view(torch.int32) >> 23) & 0xFF).to(torch.uint8)
+    return scale, code
+
+
+def _e4m3(x: torch.Tensor) -> torch.Tensor:
+    return x.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _e2m1(v: torch.Tensor) -> torch.Tensor:
+    """Nearest e2m1 code of each value (ties to the even code, saturating at 6)."""
+    a = v.abs()
+    c = ((a > 0.25).int() + (a >= 0.75).int() + (a > 1.25).int() + (a >= 1.75).int()
+         + (a > 2.5).int() + (a >= 3.5).int() + (a > 5.0).int())
+    return (c + torch.where(v < 0, 8, 0)).to(torch.uint8)
+
+
+def quantize_fmt(x: torch.Tensor, fmt: str) -> tuple[torch.Tensor, torch.Tensor]:
+    """bf16 [N, 512] -> (data rows uint8 [N, data_bytes], scale rows uint8 [N, scale_bytes])."""
+    assert x.dtype == torch.bfloat16 and x.shape[-1] == 512
+    n = x.shape[0]
+    xf = x.float()
+    if fmt == "v4":
+        g = xf[:, :448].view(n, 7, 64)
+        scale, code = _e8m0_codes(g.abs().amax(-1))
+        data = torch.empty(n, 576, dtype=torch.uint8, device=x.device)
+        data[:, :448] = _e4m3(g / scale[..., None]).view(n, 448)
+        data[:, 448:] = x[:, 448:].contiguous().view(torch.uint8).view(n, 128)
+        sc = torch.zeros(n, 8, dtype=torch.uint8, device=x.device)
+        sc[:, :7] = code
+        return data, sc
+    if fmt == "v41":
+        g = xf.view(n, 16, 32)
+        scale, code = _e8m0_codes(g.abs().amax(-1))
+        return _e4m3(g / scale[..., None]).view(n, 512), code.contiguous()
+    if fmt == "v41_fp4":
+        g = xf.view(n, 32, 16)
+        amax = g.abs().amax(-1)
+        s8 = torch.where(amax == 0, torch.ones_like(amax), amax / 6.0).to(torch.float8_e4m3fn)
+        s = s8.float()
+        codes = _e2m1(g / s[..., None]).view(n, 512)
+        data = codes[:, 0::2] | (codes[:, 1::2] << 4)
+        return data.contiguous(), s8.view(torch.uint8).contiguous()
+    raise ValueError(fmt)
+
+
+def make_pool_fmt(num_blocks: int, fmt: str, gen: torch.Generator, device,
+                  chunk_pages: int = 1 << 14) -> torch.Tensor:
+    """uint8 [num_blocks, 64 * (data + scale bytes)]: each page's data rows, then scale rows."""
+    db, sb = FMT_BYTES[fmt]
+    pool = torch.empty(num_blocks, PAGE * (db + sb), dtype=torch.uint8, device=device)
+    for lo in range(0, num_blocks, chunk_pages):
+        hi = min(num_blocks, lo + chunk_pages)
+        x = torch.randn((hi - lo) * PAGE, 512, generator=gen, device=device).to(torch.bfloat16)
+        data, sc = quantize_fmt(x, fmt)
+        pool[lo:hi, :PAGE * db] = data.view(hi - lo, PAGE * db)
+        pool[lo:hi, PAGE * db:] = sc.view(hi - lo, PAGE * sb)
+    return pool
+
+
 def _gen(device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)
@@ -166,8 +247,11 @@ def make(spec: Spec, device="cpu", gen_device=None) -> Workload:
     gd = torch.device(gen_device) if gen_device is not None else device
     gen = _gen(gd, spec.seed)
     b, s_q, h, k = spec.b, spec.s_q, spec.h_q, spec.topk
-    q = torch.randn(b, s_q, h, D_QK, generator=gen, device=gd).to(torch.bfloat16)
-    kv = make_pool(spec.num_blocks, spec.ue8m0, gen, gd)
+    q = torch.randn(b, s_q, h, spec.d_qk, generator=gen, device=gd).to(torch.bfloat16)
+    if spec.kv_format == "v32":
+        kv = make_pool(spec.num_blocks, spec.ue8m0, gen, gd)
+    else:
+        kv = make_pool_fmt(spec.num_blocks, spec.kv_format, gen, gd)
     perm = torch.randperm(spec.num_blocks, generator=gen, device=gd)
     block_table = perm[: b * spec.pages_per_seq].view(b, spec.pages_per_seq).to(torch.int32)
     rows = b * s_q
@@ -191,18 +275,18 @@ def make(spec: Spec, device="cpu", gen_device=None) -> Workload:
         phys = phys.scatter(1, which, -1)
     indices = phys.to(torch.int32).view(b, s_q, k)
     wl = Workload(spec, q.to(device), kv.to(device), indices.to(device),
-                  block_table.to(device), 1.0 / math.sqrt(D_QK))
+                  block_table.to(device), 1.0 / math.sqrt(spec.d_qk))
     return wl
 
 
 def small(b=2, s_q=1, h_q=128, topk=128, ctx=512, ue8m0=False, masked_per_row=0,
           causal_base=None, sort_indices=False, extra_pool_pages=0, seed=0,
-          device="cpu") -> Workload:
+          device="cpu", kv_format="v32") -> Workload:
     """A scaled-down workload with the same structure (for parity tests)."""
-    spec = Spec(f"small_b{b}_sq{s_q}_h{h_q}_k{topk}_ctx{ctx}", b=b, s_q=s_q, h_q=h_q,
-                topk=topk, ctx=ctx, ue8m0=ue8m0, masked_per_row=masked_per_row,
+    spec = Spec(f"small_b{b}_sq{s_q}_h{h_q}_k{topk}_ctx{ctx}_{kv_format}", b=b, s_q=s_q,
+                h_q=h_q, topk=topk, ctx=ctx, ue8m0=ue8m0, masked_per_row=masked_per_row,
                 causal_base=causal_base, sort_indices=sort_indices,
-                extra_pool_pages=extra_pool_pages, seed=seed)
+                extra_pool_pages=extra_pool_pages, seed=seed, kv_format=kv_format)
     return make(spec, device=device)
 
 
@@ -280,14 +364,19 @@ def to_numpy_inputs(wl: Workload):
     return q, kv, idx
 
 
+def row_bytes(spec: Spec) -> int:
+    """Bytes of one cached token in the spec's format (data + scales)."""
+    return ROW_BYTES if spec.kv_format == "v32" else sum(FMT_BYTES[spec.kv_format])
+
+
 def flops_valid(wl: Workload) -> float:
-    """Algorithmic FLOPs: 2 * h * (576 + 512) per valid slot (an FMA counts 2)."""
-    return 2.0 * wl.spec.h_q * (D_QK + D_V) * wl.num_valid
+    """Algorithmic FLOPs: 2 * h * (d_qk + 512) per valid slot (an FMA counts 2)."""
+    return 2.0 * wl.spec.h_q * (wl.spec.d_qk + D_V) * wl.num_valid
 
 
 def alg_bytes(wl: Workload) -> float:
     """Algorithmic HBM bytes: gathered rows + Q + O + indices + LSE per query token."""
     tok = wl.spec.b * wl.spec.s_q
     h = wl.spec.h_q
-    return (wl.num_valid * ROW_BYTES + tok * (h * D_QK * 2 + h * D_V * 2 + wl.spec.topk * 4
-                                              + h * 4))
+    return (wl.num_valid * row_bytes(wl.spec)
+            + tok * (h * wl.spec.d_qk * 2 + h * D_V * 2 + wl.spec.topk * 4 + h * 4))
