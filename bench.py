@@ -280,7 +280,7 @@ def measure_decode(spec, wl, dev, steps: int, warmup: int, flush, gpu_index: int
     import sparse_mla_attention_decode_gb300 as smla
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     op = smla.SparseMLADecode(spec.b, spec.s_q, spec.h_q, spec.topk, wl.kv.shape[0], device=dev,
-                              num_sms=num_sms)
+                              num_sms=num_sms, kv_format=spec.kv_format)
     out = torch.empty(spec.b, spec.s_q, spec.h_q, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(spec.b, spec.h_q, spec.s_q, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -641,7 +641,7 @@ def main():
     per_config = None
     if ws == 1 and not args.no_per_config:
         per_config = {}
-        for name, cfg in workloads.CONFIGS.items():
+        for name, cfg in list(workloads.CONFIGS.items()) + list(workloads.FORMAT_CONFIGS.items()):
             if name == args.workload:
                 continue
             wl_c = workloads.make(cfg, device=dev)
@@ -650,7 +650,9 @@ def main():
             del wl_c, r
             torch.cuda.empty_cache()
 
-    spec = workloads.CONFIGS[args.workload]
+    # the headline is one of the five configurations; a later-format workload may be named
+    # too (for a profiling capture of that instance)
+    spec = workloads.CONFIGS.get(args.workload) or workloads.FORMAT_CONFIGS[args.workload]
     wl = workloads.make(spec, device=dev)
     r = measure_decode(spec, wl, dev, args.steps, args.warmup, flush, local, barrier)
     op, out, lse = r["op"], r["out"], r["lse"]
@@ -740,7 +742,7 @@ def main():
     d2h = o_h[0].numel() * o_h[0].element_size() + l_h[0].numel() * l_h[0].element_size()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and spec.kv_format == "v32":
         import oracle
         oracle.build()
         r = time_oracle(wl, args.cpu_budget)

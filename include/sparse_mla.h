@@ -83,14 +83,38 @@ typedef struct {
   int32_t b;               /* batch (requests) */
   int32_t s_q;             /* query tokens per request */
   int32_t h_q;             /* query heads: 64 or 128 */
-  int32_t d_qk;            /* 576 = 512 NoPE + 64 RoPE */
+  int32_t d_qk;            /* 576 = 512 NoPE + 64 RoPE (SMLA_KV_V32), 512 (later formats) */
   int32_t d_v;             /* 512 */
   int32_t topk;            /* index slots per query token */
   int32_t page_block_size; /* 64 tokens per cache page */
   int64_t num_blocks;      /* pages in the KV cache pool; num_blocks * 64 <= 2^31 - 1 */
   int32_t extra_topk;      /* index slots per query token in the extra list (0: none) */
   int64_t extra_num_blocks; /* pages in the extra KV cache pool; * 64 <= 2^31 - 1 */
+  int32_t kv_format;       /* SMLA_KV_*: layout of kv_cache (0, the 656-byte row, by default) */
+  int32_t extra_kv_format; /* layout of the extra cache: SMLA_KV_V32 beside a V32 cache,
+                              SMLA_KV_V41_FP4 beside a V41 cache (V4: no extra cache) */
 } smla_dims;
+
+/* KV-cache formats ("FlashMLA 与 DSA", sections 3.1, 2.1, 6.1 and 6.4; the second page, step
+ * 2.3, maps d_qk = 576 to the V3.2 model and 512 to the later one).  The later formats store a
+ * page of 64 tokens as structure-of-arrays: the 64 data rows, then the 64 scale rows; token id
+ * t is row t % 64 of page t / 64, and with d_qk = d_v = 512 the value is the whole key.
+ *   SMLA_KV_V32      656 bytes a token, one row: 512 e4m3 | 4 fp32 scales (per 128) | 64 bf16
+ *                    RoPE; d_qk = 576, the value is the first 512 dims
+ *   SMLA_KV_V4       584 bytes a token: data 448 e4m3 (NoPE) | 64 bf16 (RoPE); scales 7 e8m0
+ *                    (per 64 NoPE dims) | 1 pad byte; d_qk = 512
+ *   SMLA_KV_V41      528 bytes a token: data 512 e4m3; scales 16 e8m0 (per 32 dims); d_qk = 512
+ *   SMLA_KV_V41_FP4  288 bytes a token: data 512 e2m1, two per byte (the even element in the
+ *                    low nibble); scales 32 e4m3 (per 16 dims); only as the extra cache of a
+ *                    V41 cache
+ * The byte counts are the pages'; the split of each count into fields is the reading that
+ * meets all of them.  e8m0 = 2^(e - 127) (0xFF is NaN).  The kernels multiply the dequantized
+ * keys by 256 in fp16: an e8m0 scale outside [2^-22, 2^7] or an FP4 scale above 255 sets
+ * SMLA_DEV_SCALE_RANGE. */
+#define SMLA_KV_V32 0
+#define SMLA_KV_V4 1
+#define SMLA_KV_V41 2
+#define SMLA_KV_V41_FP4 3
 
 /*
  * sparse_mla_workspace_size -- sizes of the two caller-owned device buffers.

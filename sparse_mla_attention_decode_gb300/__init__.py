@@ -39,6 +39,9 @@ SMLA_ERR_WORKSPACE = 4
 SMLA_ERR_TIMEOUT = 6
 SMLA_DEV_TIMEOUT, SMLA_DEV_Q_RANGE, SMLA_DEV_SCALE_RANGE, SMLA_DEV_TOPK_TABLE = 0x1, 0x2, 0x4, 0x8
 SMLA_DEV_NAN_INPUT = 0x10
+# cache formats of smla_dims.kv_format / extra_kv_format
+SMLA_KV_V32, SMLA_KV_V4, SMLA_KV_V41, SMLA_KV_V41_FP4 = 0, 1, 2, 3
+_KV_FORMATS = {"v32": SMLA_KV_V32, "v4": SMLA_KV_V4, "v41": SMLA_KV_V41}
 SMLA_SCORES_BF16, SMLA_SCORES_FP32 = 0, 1
 EXPORTED = ["sparse_mla_workspace_size", "sparse_mla_sched_meta", "sparse_mla_decode_fwd",
             "sparse_mla_combine", "sparse_mla_status_string", "sparse_mla_read_device_status",
@@ -62,7 +65,8 @@ class smla_dims(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int32), ("s_q", ctypes.c_int32), ("h_q", ctypes.c_int32),
                 ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("page_block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
-                ("extra_topk", ctypes.c_int32), ("extra_num_blocks", ctypes.c_int64)]
+                ("extra_topk", ctypes.c_int32), ("extra_num_blocks", ctypes.c_int64),
+                ("kv_format", ctypes.c_int32), ("extra_kv_format", ctypes.c_int32)]
 
 
 class smla_decode_opts(ctypes.Structure):
@@ -359,15 +363,22 @@ def sparse_mla_read_device_status(dims: smla_dims, num_sms: int, sched_meta: int
 
 
 def dims_for(b: int, s_q: int, h_q: int, topk: int, num_blocks: int, extra_topk: int = 0,
-             extra_num_blocks: int = 0) -> smla_dims:
-    return smla_dims(b, s_q, h_q, 576, 512, topk, 64, num_blocks, extra_topk, extra_num_blocks)
+             extra_num_blocks: int = 0, kv_format: str = "v32") -> smla_dims:
+    """Problem sizes; kv_format "v32" (656-byte rows, d_qk 576), "v4" or "v41" (d_qk 512; the
+    extra cache of a "v41" cache is FP4)."""
+    f = _KV_FORMATS[kv_format]
+    return smla_dims(b, s_q, h_q, 576 if f == SMLA_KV_V32 else 512, 512, topk, 64, num_blocks,
+                     extra_topk, extra_num_blocks, f,
+                     SMLA_KV_V41_FP4 if f == SMLA_KV_V41 else SMLA_KV_V32)
 
 
 class SparseMLADecode:
     """Owns the plan and workspace buffers of one problem shape and runs the three calls.
 
-    q: bf16 [b, s_q, h_q, 576]; kv_cache: uint8 [num_blocks, 64, 1, 656]; indices: int32
-    [b, s_q, topk]; returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, h_q, s_q]).
+    q: bf16 [b, s_q, h_q, d_qk]; kv_cache: uint8 pages (656-byte rows, [num_blocks, 64, 1,
+    656], or ``kv_format`` "v4" / "v41": [num_blocks, 64 * 584] / [num_blocks, 64 * 528], data
+    rows then scale rows); indices: int32 [b, s_q, topk]; returns (out bf16 [b, s_q, h_q,
+    512], lse fp32 [b, h_q, s_q]).
     Optional ``attn_sink`` (fp32 [h_q]) and ``topk_length`` (int32 [b, s_q]) device tensors
     and ``partials_bf16`` select the decode variants of ``smla_decode_opts``; a problem built
     with ``extra_topk`` > 0 takes ``extra_kv`` (uint8 [extra_num_blocks, 64, 1, 656]),
@@ -375,13 +386,15 @@ class SparseMLADecode:
     """
 
     def __init__(self, b: int, s_q: int, h_q: int, topk: int, num_blocks: int, device=None,
-                 num_sms: int = 0, extra_topk: int = 0, extra_num_blocks: int = 0):
+                 num_sms: int = 0, extra_topk: int = 0, extra_num_blocks: int = 0,
+                 kv_format: str = "v32"):
         import torch
         self.device = torch.device(device if device is not None else "cuda")
         if num_sms <= 0:
             num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.num_sms = int(num_sms)
-        self.dims = dims_for(b, s_q, h_q, topk, num_blocks, extra_topk, extra_num_blocks)
+        self.dims = dims_for(b, s_q, h_q, topk, num_blocks, extra_topk, extra_num_blocks,
+                             kv_format)
         sb, ab = sparse_mla_workspace_size(self.dims, self.num_sms)
         self.sched_bytes, self.accum_bytes = sb, ab
         self.sched = torch.empty(max(sb, 16), dtype=torch.uint8, device=self.device)

@@ -27,7 +27,19 @@ smla_status check_dims(const smla_dims* d) {
       d->extra_num_blocks < 0)
     return SMLA_ERR_INVALID_ARG;
   if (d->h_q != 64 && d->h_q != 128) return SMLA_ERR_UNSUPPORTED;
-  if (d->d_qk != kDQk || d->d_v != kDV || d->page_block_size != kPage) return SMLA_ERR_UNSUPPORTED;
+  if (d->d_v != kDV || d->page_block_size != kPage) return SMLA_ERR_UNSUPPORTED;
+  // the cache format fixes d_qk: 576 for the 656-byte rows, 512 for the later formats; the
+  // extra cache is 656-byte beside a 656-byte cache and FP4 beside a V4.1 cache (V4: none)
+  if (d->kv_format == SMLA_KV_V32) {
+    if (d->d_qk != kDQk || d->extra_kv_format != SMLA_KV_V32) return SMLA_ERR_UNSUPPORTED;
+  } else if (d->kv_format == SMLA_KV_V4) {
+    if (d->d_qk != 512 || d->extra_topk != 0) return SMLA_ERR_UNSUPPORTED;
+  } else if (d->kv_format == SMLA_KV_V41) {
+    if (d->d_qk != 512 || (d->extra_topk != 0 && d->extra_kv_format != SMLA_KV_V41_FP4))
+      return SMLA_ERR_UNSUPPORTED;
+  } else {
+    return SMLA_ERR_UNSUPPORTED;
+  }
   if (d->num_blocks * static_cast<int64_t>(kPage) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
   if (d->extra_num_blocks * static_cast<int64_t>(kPage) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
   if (plan_topk(d) > INT32_MAX) return SMLA_ERR_UNSUPPORTED;
@@ -258,7 +270,7 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   const PlanLayout L = plan_layout(dims->b, parts);
   const uint8_t* plan = static_cast<const uint8_t*>(sched_meta);
   DecodeParams p;
-  if (!encode_rows_map(&p.q_map, q, false, tokens * dims->h_q, kDQk, 64, dims->h_q) ||
+  if (!encode_rows_map(&p.q_map, q, false, tokens * dims->h_q, dims->d_qk, 64, dims->h_q) ||
       !encode_rows_map(&p.out_map, out, false, tokens * dims->h_q, kDV, 64, dims->h_q))
     return SMLA_ERR_CUDA;
   if (A.max_splits > 0) {
@@ -306,6 +318,8 @@ smla_status sparse_mla_decode_fwd_ex(const smla_dims* dims, int num_sms, const v
   p.nb_main = (dims->topk + kPage - 1) / kPage;
   p.nb_total = static_cast<int>((plan_topk(dims) + kPage - 1) / kPage);
   p.num_rows = static_cast<int>(dims->num_blocks * kPage);
+  p.kv_fmt = dims->kv_format == SMLA_KV_V4 ? FMT_V4 : dims->kv_format == SMLA_KV_V41 ? FMT_V41 : FMT_V32;
+  p.q_chunks = dims->d_qk / 64;
   p.store32 = aligned(out, 32) && (A.max_splits == 0 || aligned(workspace, 32)) ? 1 : 0;
   p.score_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634 / 256.0);
   return cuda_status(launch_decode(p, parts, s));

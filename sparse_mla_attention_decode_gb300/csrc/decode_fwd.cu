@@ -222,11 +222,18 @@ struct Cursor {
 // warp is in flight and no row passes through registers before it has landed.  A slot whose
 // index is masked is zero-filled without a read.
 constexpr int RING = 8;  // row slots per dequant warp
-template <bool kScores>
+// Ring slot of one gathered row: the 656-byte row (S-CTA) or its NoPE codes + scales (O-CTA);
+// for the later formats (both CTAs: the value is the whole key) the data row, then its scale
+// row padded to 16 bytes.
+template <bool kScores, int kF>
 struct RowCopy {
-  static constexpr int kBytes = kScores ? kRowBytes : kDNope + 16;  // 656 or 528 bytes per slot
+  static constexpr int kBytes = kF == FMT_V32 ? (kScores ? kRowBytes : kDNope + 16)
+                                              : FmtBytes<kF>::kData + 16;
 };
-static_assert(8 * RING * RowCopy<true>::kBytes <= RAW_BYTES, "row ring");
+static_assert(8 * RING * RowCopy<true, FMT_V32>::kBytes <= RAW_BYTES &&
+                  8 * RING * RowCopy<true, FMT_V4>::kBytes <= RAW_BYTES &&
+                  8 * RING * RowCopy<true, FMT_V41>::kBytes <= RAW_BYTES,
+              "row ring");
 
 // Index of one slot, -1 for a slot past the list or (kLen: the kernel instance for per-token
 // lengths) past the token's topk_length; both loads are issued before either is tested.  The
@@ -321,11 +328,166 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
   }
 }
 
+// ---- the later formats (d_qk = d_v = 512, structure-of-arrays pages; "FlashMLA 与 DSA",
+// sections 3.1, 2.1 and 6.4).  A page of 64 tokens holds the 64 data rows, then the 64 scale
+// rows.  V4: 448 e4m3 codes (e8m0 scale per 64 dims) + 64 bf16 RoPE values, 8 scale bytes
+// (7 + 1 pad); V4.1: 512 e4m3 codes, 16 e8m0 scales (per 32 dims); FP4 (the extra cache of a
+// V4.1 cache only): 512 e2m1 values, two per byte with the even element in the low nibble, and
+// 32 e4m3 scales (per 16 dims).  The value is the whole key, so both CTAs convert the same
+// eight 64-dim chunks.
+
+// Copies this lane's share of one row of a later format into its ring slot: data unit
+// (16 bytes) j + 8 k, and the scale row (lane 0; FP4: lanes 0 and 1).  An invalid id reads
+// nothing and zero-fills.  One commit group per call.
+template <int kF>
+__device__ __forceinline__ void issue_row_soa(const DecodeParams& p, int32_t idx, uint32_t slot,
+                                              int j, bool extra) {
+  const bool fp4 = kF == FMT_V41 && extra;
+  const int data = fp4 ? FP4_DATA : FmtBytes<kF>::kData;
+  const int scale = fp4 ? FP4_SCALE : FmtBytes<kF>::kScale;
+  const uint8_t* base = extra ? p.extra_kv : p.kv;
+  const bool ok = idx >= 0 && idx < (extra ? p.extra_rows : p.num_rows);
+  const uint32_t t = ok ? static_cast<uint32_t>(idx) : 0u;
+  const uint8_t* page = base + static_cast<size_t>(t >> 6) * (kPage * (data + scale));
+  const uint8_t* src = page + (t & 63u) * data;
+  const uint8_t* ssrc = page + kPage * data + (t & 63u) * scale;
+  const uint32_t n = ok ? 16u : 0u;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int u = j + 8 * k;
+    if (u < data / 16) cp_async16(slot + u * 16, src + u * 16, n);
+  }
+  if (kF == FMT_V4 && !fp4) {
+    if (j == 0) cp_async8(slot + data, ssrc, ok ? 8u : 0u);
+  } else if (fp4) {
+    if (j < 2) cp_async16(slot + data + 16 * j, ssrc + 16 * j, n);
+  } else if (j == 0) {
+    cp_async16(slot + data, ssrc, n);
+  }
+  cp_async_commit();
+}
+
+// This lane's share of a landed row: a[k] = data unit j + 8 k (V4: units j + 24 only for
+// j < 4, c = RoPE unit 28 + j; FP4: a[0], a[1] = units j, j + 8), b = the scale row (FP4: the
+// scale pairs 2 j, 2 j + 1 and 2 j + 16, 2 j + 17 in b.x).
+template <int kF>
+__device__ __forceinline__ void load_row_soa(uint32_t slot, int j, bool extra, uint4 (&a)[4],
+                                             uint4& b, uint4& c) {
+  if (kF == FMT_V41 && extra) {
+    ld_shared_v4(slot + j * 16, a[0].x, a[0].y, a[0].z, a[0].w);
+    ld_shared_v4(slot + (j + 8) * 16, a[1].x, a[1].y, a[1].z, a[1].w);
+    b.x = ld_shared_u16(slot + FP4_DATA + 2 * j) | (ld_shared_u16(slot + FP4_DATA + 16 + 2 * j) << 16);
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (kF == FMT_V4 && k == 3 && j >= 4) {
+      a[k] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    ld_shared_v4(slot + (j + 8 * k) * 16, a[k].x, a[k].y, a[k].z, a[k].w);
+  }
+  if (kF == FMT_V4) {
+    ld_shared_v4(slot + (28 + j) * 16, c.x, c.y, c.z, c.w);
+    ld_shared_v2(slot + FmtBytes<kF>::kData, b.x, b.y);
+  } else {
+    ld_shared_v4(slot + FmtBytes<kF>::kData, b.x, b.y, b.z, b.w);
+  }
+}
+
+// 256 x an e8m0 scale as an f16x2 pair: 2^(e - 127 + 8) is the fp16 with exponent field
+// e - 104 (normal for e in [105, 134]; others are flagged and clamped); 0xFF is NaN.
+__device__ __forceinline__ uint32_t e8m0_x256_f16x2(uint32_t e, uint32_t& bad) {
+  if (e == 255u) return F16_NAN2;
+  const int ex = static_cast<int>(e) - 104;
+  bad |= ex < 1 || ex > 30;
+  const uint32_t h = static_cast<uint32_t>(ex < 1 ? 1 : (ex > 30 ? 30 : ex)) << 10;
+  return h | (h << 16);
+}
+
+// Converts this lane's share of a landed row of a later format into the fp16 tile (row `row`,
+// eight 64-dim chunks); invalid: NaN key (S-CTA) or zero value (O-CTA).
+template <bool kScores, int kF>
+__device__ __forceinline__ void store_row_soa(uint32_t tile, int row, int j, bool valid, bool extra,
+                                              const uint4 (&a)[4], const uint4& b, const uint4& c,
+                                              uint32_t& bad) {
+  const uint32_t flip = (j >> 2) & 1;
+  const uint32_t u0 = 2 * (j & 3) + flip, u1 = 2 * (j & 3) + (flip ^ 1u);
+  const uint32_t ch0 = tile + (j >> 2) * CHUNK;
+  if (!valid) {
+    const uint32_t f = kScores ? F16_NAN2 : 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      st_shared_v4(ch0 + 2 * k * CHUNK + sw128_chunk(row, u0), f, f, f, f);
+      st_shared_v4(ch0 + 2 * k * CHUNK + sw128_chunk(row, u1), f, f, f, f);
+    }
+    return;
+  }
+  if (kF == FMT_V41 && extra) {  // FP4: units j and j + 8, 32 dims each (4 sub-chunks)
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+      const int u = j + 8 * uu;
+      // the unit's two e4m3 scales (16 dims each) x 256 as fp16; 256 x 448 would overflow
+      const uint32_t s2 = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(uu ? b.x >> 16 : b.x & 0xFFFFu)),
+                                0x5C005C00u);
+      bad |= ((s2 & 0x7FFFu) == 0x7C00u) | (((s2 >> 16) & 0x7FFFu) == 0x7C00u);
+      const uint32_t slo = (s2 & 0xFFFFu) * 0x10001u, shi = (s2 >> 16) * 0x10001u;
+      const uint32_t wd[4] = {a[uu].x, a[uu].y, a[uu].z, a[uu].w};
+      const uint32_t ch = tile + (u >> 1) * CHUNK;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {  // word m: dims 32 u + 8 m .. + 8 (scale 2 u + m / 2)
+        const uint32_t sc = m < 2 ? slo : shi;
+        st_shared_v4(ch + sw128_chunk(row, (u & 1) * 4 + m),
+                     hmul2(cvt_e2m1x2_f16x2(wd[m] & 0xFFu), sc),
+                     hmul2(cvt_e2m1x2_f16x2((wd[m] >> 8) & 0xFFu), sc),
+                     hmul2(cvt_e2m1x2_f16x2((wd[m] >> 16) & 0xFFu), sc),
+                     hmul2(cvt_e2m1x2_f16x2(wd[m] >> 24), sc));
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // code unit j + 8 k -> chunk j / 4 + 2 k, as the 656-byte NoPE
+    if (kF == FMT_V4 && k == 3 && j >= 4) continue;  // units 28-31 are RoPE, converted below
+    uint32_t e;
+    if (kF == FMT_V41) {  // scale of dims 32 s..: s = (j + 8 k) / 2 = j / 2 + 4 k
+      const uint32_t wk = k == 0 ? b.x : k == 1 ? b.y : k == 2 ? b.z : b.w;
+      e = (wk >> (8 * ((j >> 1) & 3))) & 0xFFu;
+    } else {  // V4: scale of dims 64 s..: s = j / 4 + 2 k
+      const int si = (j >> 2) + 2 * k;
+      e = ((si < 4 ? b.x : b.y) >> (8 * (si & 3))) & 0xFFu;
+    }
+    const uint32_t sc2 = e8m0_x256_f16x2(e, bad);
+    const uint32_t w[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      o[2 * q] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[q] & 0xFFFFu)), sc2);
+      o[2 * q + 1] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[q] >> 16)), sc2);
+    }
+    const uint32_t ch = ch0 + 2 * k * CHUNK;
+    st_shared_v4(ch + sw128_chunk(row, u0), flip ? o[4] : o[0], flip ? o[5] : o[1],
+                 flip ? o[6] : o[2], flip ? o[7] : o[3]);
+    st_shared_v4(ch + sw128_chunk(row, u1), flip ? o[0] : o[4], flip ? o[1] : o[5],
+                 flip ? o[2] : o[6], flip ? o[3] : o[7]);
+  }
+  if (kF == FMT_V4) {  // RoPE unit j: dims 448 + 8 j .. + 8 (bf16 -> 256 x fp16), chunk 7
+    const uint32_t r[4] = {c.x, c.y, c.z, c.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      q[e] = pack_f16x2(__uint_as_float(r[e] << 16) * 256.f,
+                        __uint_as_float(r[e] & 0xFFFF0000u) * 256.f);
+    st_shared_v4(tile + 7 * CHUNK + sw128_chunk(row, j), q[0], q[1], q[2], q[3]);
+  }
+}
+
 // kExtra: the kernel instance with an extra cache, whose blocks follow the main list's in the
-// plan (blocks nb_main and up read the extra indices and rows).
-template <bool kScores, bool kLen, bool kExtra>
+// plan (blocks nb_main and up read the extra indices and rows).  kF: the main cache's format
+// (the extra cache of a V4.1 cache is FP4; of a 656-byte cache, 656-byte).
+template <bool kScores, bool kLen, bool kExtra, int kF>
 __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl, int t) {
-  using RC = RowCopy<kScores>;
+  using RC = RowCopy<kScores, kF>;
   const int w = t >> 5, lane = t & 31;  // warp w of the 8 dequant warps
   const int j = lane & 7, rsel = lane >> 3;
   const int bfull = kScores ? B_KT_FULL : B_VT_FULL;
@@ -353,7 +515,11 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = 4 * h + rsel;
-    issue_rows<kScores>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j,
+    if (kF == FMT_V32)
+      issue_rows<kScores>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j,
+                          in_extra(fetch));
+    else
+      issue_row_soa<kF>(p, __shfl_sync(0xffffffffu, ix0, r), ring + r * RC::kBytes, j,
                         in_extra(fetch));
   }
   fetch.next(pl);
@@ -367,6 +533,7 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     ah.next(pl);
     const bool issue_more = !ah.done(pl);  // block cur + 1 exists
     const bool extra_next = in_extra(ah);
+    const bool extra_cur = in_extra(cur);
     const int32_t ixB = idx_of(fetch);      // block cur + 2, loaded one block early
     vmask |= valid_bits(ixA, extra_next) << 8;
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
@@ -382,17 +549,29 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
         cp_async_wait<1>();          // the copies of this step (the older group) have landed
         __syncwarp();
         const uint32_t slot = ring + r * RC::kBytes;
-        uint4 nope[4], scales, rope = make_uint4(0u, 0u, 0u, 0u);
+        uint4 nope[4], scales = make_uint4(0u, 0u, 0u, 0u), rope = make_uint4(0u, 0u, 0u, 0u);
+        if (kF == FMT_V32) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          ld_shared_v4(slot + (j + 8 * k) * 16, nope[k].x, nope[k].y, nope[k].z, nope[k].w);
-        ld_shared_v4(slot + kDNope, scales.x, scales.y, scales.z, scales.w);
-        if (kScores) ld_shared_v4(slot + kDNope + 16 + j * 16, rope.x, rope.y, rope.z, rope.w);
+          for (int k = 0; k < 4; ++k)
+            ld_shared_v4(slot + (j + 8 * k) * 16, nope[k].x, nope[k].y, nope[k].z, nope[k].w);
+          ld_shared_v4(slot + kDNope, scales.x, scales.y, scales.z, scales.w);
+          if (kScores) ld_shared_v4(slot + kDNope + 16 + j * 16, rope.x, rope.y, rope.z, rope.w);
+        } else {
+          load_row_soa<kF>(slot, j, extra_cur, nope, scales, rope);
+        }
         __syncwarp();  // every lane has read the slot: it can take the next block's row
         const int32_t nx = __shfl_sync(0xffffffffu, ixA, r);
-        if (issue_more) issue_rows<kScores>(p, nx, slot, j, extra_next);
-        else cp_async_commit();  // an empty group keeps the count per step uniform
-        store_rows<kScores>(tile, w + 8 * r, j, (vmask >> r) & 1u, nope, scales, rope, bad);
+        if (issue_more) {
+          if (kF == FMT_V32) issue_rows<kScores>(p, nx, slot, j, extra_next);
+          else issue_row_soa<kF>(p, nx, slot, j, extra_next);
+        } else {
+          cp_async_commit();  // an empty group keeps the count per step uniform
+        }
+        if (kF == FMT_V32)
+          store_rows<kScores>(tile, w + 8 * r, j, (vmask >> r) & 1u, nope, scales, rope, bad);
+        else
+          store_row_soa<kScores, kF>(tile, w + 8 * r, j, (vmask >> r) & 1u, extra_cur, nope,
+                                     scales, rope, bad);
       }
     }
     // the block's validity bits for the softmax (this warp's byte of all 32 rows); the MMA
@@ -413,8 +592,10 @@ out:
 }
 
 // ---------------------------------------------------------------------------------------
-// S-CTA MMA warp: S[buf] = Q K^T for every block (36 MMAs of K = 16).  The whole warp runs
+// S-CTA MMA warp: S[buf] = Q K^T for every block (4 MMAs of K = 16 per 64-dim chunk: 36 at
+// d_qk = 576, 32 at 512).  The whole warp runs
 // the loop (waits included) and one elected lane issues each MMA and commit.
+template <int kChunks>
 __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bool stall) {
   // test hook: a wait that nothing ends, so every role runs into its bounded wait
   if (stall) {
@@ -437,7 +618,7 @@ __device__ void role_mma_scores(const Ctx& c, const Plan& pl, uint32_t tbase, bo
       const uint64_t bdesc = umma_desc(c.sbase + OFF_TILE + st * KT_STAGE, 16, 1024, 2);
       const uint32_t d = tbase + TM_S + sb * BT;
 #pragma unroll 4  // kept rolled: the issuing warp shares its instruction cache with the others
-      for (int kk = 0; kk < 36; ++kk)  // descriptor start addresses advance in 16-byte units
+      for (int kk = 0; kk < 4 * kChunks; ++kk)  // descriptor start addresses advance in 16 bytes
         mma_ts_warp(d, tbase + TM_Q + kk * 8,
                     bdesc + ((((kk >> 2) * CHUNK) + (kk & 3) * 32) >> 4), IDESC_QK, kk > 0);
       mma_commit_warp(c.bar(B_S_FULL + sb));
@@ -493,8 +674,9 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
                              uint32_t& bad, uint32_t item) {
   const uint32_t qs = c.sbase + OFF_TILE;
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
+  const int nch = p.q_chunks;
   if (i == 0) {
-    for (int ch = 0; ch < 9; ++ch) {
+    for (int ch = 0; ch < nch; ++ch) {
       mbar_arrive_expect_tx(c.bar(B_QLOAD + ch), chunk_bytes);
       tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD + ch));
     }
@@ -504,7 +686,7 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
   const uint32_t sw = static_cast<uint32_t>(i & 7);
   uint32_t mag[4] = {0u, 0u, 0u, 0u};  // largest bf16 magnitude seen, per 16-bit half (4 chains)
 #pragma unroll 1
-  for (int ch = 0; ch < 9; ++ch) {
+  for (int ch = 0; ch < nch; ++ch) {
     if (!c.wait_warp(B_QLOAD + ch, item & 1)) return false;
     uint32_t w[32];
     if (live) {
@@ -932,8 +1114,8 @@ __device__ void role_relay(const Ctx& c, const Plan& pl) {
 }
 
 // kLen: per-token top-k lengths are given (p.topk_length is read); otherwise it is not.
-// kExtra: an extra cache and index list follow the main ones.
-template <bool kLen, bool kExtra>
+// kExtra: an extra cache and index list follow the main ones.  kF: the cache format.
+template <bool kLen, bool kExtra, int kF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1015,10 +1197,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       if (scores) role_softmax(p, c, pl, tbase, threadIdx.x);
       else role_values_epilogue(p, c, pl, tbase, threadIdx.x);
     } else if (dq >= 0) {
-      if (scores) role_dequant<true, kLen, kExtra>(p, c, pl, dq * 32 + lane);
-      else role_dequant<false, kLen, kExtra>(p, c, pl, dq * 32 + lane);
+      if (scores) role_dequant<true, kLen, kExtra, kF>(p, c, pl, dq * 32 + lane);
+      else role_dequant<false, kLen, kExtra, kF>(p, c, pl, dq * 32 + lane);
     } else if (warp == 12) {
-      if (scores) role_mma_scores(c, pl, tbase, p.test_stall != 0);
+      if (scores) role_mma_scores<kF == FMT_V32 ? 9 : 8>(c, pl, tbase, p.test_stall != 0);
       else role_mma_values(c, pl, tbase);
       mma_commit_warp(c.bar(B_DRAIN));  // every issued MMA has finished before TMEM is freed
       if (lane == 0) c.drain(B_DRAIN, 0);
@@ -1041,10 +1223,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int parts, cudaStream_t stream) {
-  void (*kernel)(DecodeParams) =
-      p.extra_indices != nullptr
-          ? (p.topk_length != nullptr ? decode_kernel<true, true> : decode_kernel<false, true>)
-          : (p.topk_length != nullptr ? decode_kernel<true, false> : decode_kernel<false, false>);
+  const bool len = p.topk_length != nullptr, extra = p.extra_indices != nullptr;
+  void (*kernel)(DecodeParams) = nullptr;
+  if (p.kv_fmt == FMT_V32)
+    kernel = extra ? (len ? decode_kernel<true, true, FMT_V32> : decode_kernel<false, true, FMT_V32>)
+                   : (len ? decode_kernel<true, false, FMT_V32> : decode_kernel<false, false, FMT_V32>);
+  else if (p.kv_fmt == FMT_V4 && !extra)
+    kernel = len ? decode_kernel<true, false, FMT_V4> : decode_kernel<false, false, FMT_V4>;
+  else if (p.kv_fmt == FMT_V41)
+    kernel = extra ? (len ? decode_kernel<true, true, FMT_V41> : decode_kernel<false, true, FMT_V41>)
+                   : (len ? decode_kernel<true, false, FMT_V41> : decode_kernel<false, false, FMT_V41>);
+  if (kernel == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -10,6 +10,22 @@ namespace smla {
 constexpr int kDQk = 576, kDNope = 512, kDRope = 64, kDV = 512;
 constexpr int kRowBytes = 656;  // 512 e4m3 + 4 x fp32 scale + 64 x bf16
 constexpr int kPage = 64;
+// KV-cache formats of the decode kernel: the 656-byte V3.2 row (d_qk 576) and the later
+// structure-of-arrays pages (d_qk 512; the FP4 form only as the extra cache of a V4.1 cache)
+enum : int { FMT_V32 = 0, FMT_V4 = 1, FMT_V41 = 2, FMT_V41_FP4 = 3 };
+template <int kF>
+struct FmtBytes {  // bytes of one token's data row and scale row
+  static constexpr int kData = 0, kScale = 0;
+};
+template <>
+struct FmtBytes<FMT_V4> {
+  static constexpr int kData = 448 + 64 * 2, kScale = 8;
+};
+template <>
+struct FmtBytes<FMT_V41> {
+  static constexpr int kData = 512, kScale = 16;
+};
+constexpr int FP4_DATA = 256, FP4_SCALE = 32;
 constexpr int kTopkBlock = 64;  // slots of the top-k list per pipeline block
 constexpr int kFixedOverhead = 5;
 constexpr int kMetaInts = 8;    // int32 fields per partition in the plan
@@ -79,6 +95,8 @@ struct DecodeParams {
   int s_step;
   int num_rows;             // num_blocks * 64
   float score_scale_log2;   // sm_scale * log2(e) / 256 (keys are dequantized scaled by 256)
+  int kv_fmt;               // FMT_V32, FMT_V4 or FMT_V41 (the main cache)
+  int q_chunks;             // 64-dim chunks of q and of the key: 9 (d_qk 576) or 8 (512)
   int store32;              // out and the workspace are 32-byte aligned (256-bit stores)
   int partials_bf16;        // split partials of O stored as bf16 rows (else fp32)
   int test_stall;           // failure-path test hook (see smla_decode_opts)

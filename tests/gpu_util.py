@@ -24,7 +24,7 @@ def run_cuda(wl: workloads.Workload, num_sms: int = 0, check_status: bool = True
     enb = 0 if extra_kv is None else extra_kv.shape[0]
     op = smla.SparseMLADecode(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk,
                               wl.kv.shape[0], device=dev, num_sms=num_sms, extra_topk=ek,
-                              extra_num_blocks=enb)
+                              extra_num_blocks=enb, kv_format=wl.spec.kv_format)
     out, lse = op.run(wl.q, wl.kv, wl.indices, wl.sm_scale, attn_sink=attn_sink,
                       topk_length=topk_length, partials_bf16=partials_bf16, extra_kv=extra_kv,
                       extra_indices=extra_indices, extra_topk_length=extra_topk_length)
@@ -148,3 +148,25 @@ def compare(o_gpu, l_gpu, o_ref, l_ref, what: str = ""):
     assert rel <= O_REL_L2, f"{what}: rel L2 {rel}"
     assert lse_err <= LSE_ABS, f"{what}: lse abs {lse_err}"
     return {"max_abs": max_abs, "rel_l2": rel, "worst_row_rel": worst_row, "lse_abs": lse_err}
+
+
+def oracle_tokens_fmt(wl: workloads.Workload, tokens, attn_sink=None, topk_length=None,
+                      extra_kv=None, extra_indices=None, extra_topk_length=None):
+    """Later-format oracle (out [n, h, 512], lse [n, h]) for the given flattened tokens; the
+    pool is read on the host (whole), the FP4 extra cache likewise."""
+    from oracle import formats as ofmt
+    q = wl.q.cpu().contiguous().view(torch.int16).numpy().view("uint16")
+    pool = wl.kv.cpu().numpy()
+    kw = {}
+    if attn_sink is not None:
+        kw["attn_sink"] = attn_sink.double().cpu().numpy()
+    if topk_length is not None:
+        kw["topk_length"] = topk_length.cpu().numpy()
+    if extra_indices is not None:
+        kw.update(extra_pool=extra_kv.cpu().numpy(), extra_fmt="v41_fp4",
+                  extra_indices=extra_indices.cpu().numpy())
+        if extra_topk_length is not None:
+            kw["extra_topk_length"] = extra_topk_length.cpu().numpy()
+    out, lse, _ = ofmt.sparse_mla_decode_fmt(q, pool, wl.indices.cpu().numpy(), wl.sm_scale,
+                                             wl.spec.kv_format, tokens=np.asarray(tokens), **kw)
+    return out, lse

@@ -94,6 +94,22 @@ def test_bad_dims_rejected(L, field, value, code):
     assert L.sparse_mla_workspace_size(ctypes.byref(d), 152, ctypes.byref(a), ctypes.byref(b)) == code
 
 
+@pytest.mark.parametrize("fmt,d_qk,extra_topk,extra_fmt,code", [
+    ("v41", 512, 0, 3, 0), ("v41", 512, 64, 3, 0), ("v4", 512, 0, 0, 0),
+    ("v4", 512, 64, 0, 2),      # no extra cache beside a V4 cache
+    ("v41", 512, 64, 0, 2),     # the extra cache of a V4.1 cache is FP4
+    ("v32", 512, 0, 0, 2), ("v41", 576, 0, 3, 2), ("v4", 576, 0, 0, 2),
+    ("v32", 576, 64, 3, 2)])
+def test_kv_formats_checked(L, fmt, d_qk, extra_topk, extra_fmt, code):
+    d = smla.dims_for(2, 1, 128, 128, 64, extra_topk=extra_topk,
+                      extra_num_blocks=8 if extra_topk else 0, kv_format=fmt)
+    d.d_qk, d.extra_kv_format = d_qk, extra_fmt
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.sparse_mla_workspace_size(ctypes.byref(d), 152, ctypes.byref(a), ctypes.byref(b)) == code
+    d.kv_format = 7
+    assert L.sparse_mla_workspace_size(ctypes.byref(d), 152, ctypes.byref(a), ctypes.byref(b)) == 2
+
+
 def test_pointer_checks_before_launch(L):
     d = smla.dims_for(2, 1, 128, 128, 64)
     sb, ab = smla.sparse_mla_workspace_size(d, 152)

@@ -54,3 +54,7 @@ def test_committed_profiles_match_the_current_kernels():
                       ("topk.cu", "topk_kernel_prefill_1024x65536_k2048.md"),
                       ("indexer.cu", "indexer_kernel_decode_b64_ctx32768.md")):
         assert bench.traffic_from_profiles(os.path.join(csrc, src), prof) is not None, prof
+    # the selection chain's two kernels share one summary
+    assert bench.traffic_from_pair_profile(
+        [os.path.join(csrc, "indexer.cu"), os.path.join(csrc, "topk.cu")],
+        "select_kernels_decode_b64_ctx32768_k2048.md") is not None

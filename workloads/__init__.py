@@ -94,6 +94,18 @@ CONFIGS: dict[str, Spec] = {
 }
 
 
+# The decode-shaped workload in the later cache formats (d_qk = 512): measured beside the five
+# configurations above, not part of their list.
+FORMAT_CONFIGS: dict[str, Spec] = {
+    "c2fmt_b64_h128_k2048_mask5_v41": Spec("c2fmt_b64_h128_k2048_mask5_v41", b=64, s_q=1,
+                                           h_q=128, topk=2048, ctx=32768, masked_per_row=102,
+                                           seed=1, kv_format="v41"),
+    "c2fmt_b64_h128_k2048_mask5_v4": Spec("c2fmt_b64_h128_k2048_mask5_v4", b=64, s_q=1,
+                                          h_q=128, topk=2048, ctx=32768, masked_per_row=102,
+                                          seed=1, kv_format="v4"),
+}
+
+
 @dataclass
 class Workload:
     spec: Spec
