@@ -294,7 +294,10 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
       const float scale = __uint_as_float(sc[k]) * 256.f;
       bad |= !(scale >= 6.103515625e-05f && scale <= 65504.f);
       const uint32_t sc2 = pack_f16x2(scale, scale);
-      const uint32_t w[4] = {nope[k].x, nope[k].y, nope[k].z, nope[k].w};
+      // the first store goes to sub-chunk u0: the flipped lanes convert their second 8 codes
+      // first (the two 8-byte halves of the unit swapped once, instead of every output word)
+      const uint32_t w[4] = {flip ? nope[k].z : nope[k].x, flip ? nope[k].w : nope[k].y,
+                             flip ? nope[k].x : nope[k].z, flip ? nope[k].y : nope[k].w};
       uint32_t o[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -302,10 +305,8 @@ __device__ __forceinline__ void store_rows(uint32_t tile, int row, int j, bool v
         o[2 * e + 1] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[e] >> 16)), sc2);
       }
       const uint32_t ch = ch0 + 2 * k * CHUNK;
-      st_shared_v4(ch + sw128_chunk(row, u0), flip ? o[4] : o[0], flip ? o[5] : o[1],
-                   flip ? o[6] : o[2], flip ? o[7] : o[3]);
-      st_shared_v4(ch + sw128_chunk(row, u1), flip ? o[0] : o[4], flip ? o[1] : o[5],
-                   flip ? o[2] : o[6], flip ? o[3] : o[7]);
+      st_shared_v4(ch + sw128_chunk(row, u0), o[0], o[1], o[2], o[3]);
+      st_shared_v4(ch + sw128_chunk(row, u1), o[4], o[5], o[6], o[7]);
     }
     if (kScores) {
       const uint32_t r[4] = {rope.x, rope.y, rope.z, rope.w};
@@ -458,7 +459,8 @@ __device__ __forceinline__ void store_row_soa(uint32_t tile, int row, int j, boo
       e = ((si < 4 ? b.x : b.y) >> (8 * (si & 3))) & 0xFFu;
     }
     const uint32_t sc2 = e8m0_x256_f16x2(e, bad);
-    const uint32_t w[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+    const uint32_t w[4] = {flip ? a[k].z : a[k].x, flip ? a[k].w : a[k].y,
+                           flip ? a[k].x : a[k].z, flip ? a[k].y : a[k].w};
     uint32_t o[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -466,10 +468,8 @@ __device__ __forceinline__ void store_row_soa(uint32_t tile, int row, int j, boo
       o[2 * q + 1] = hmul2(cvt_e4m3x2_f16x2(static_cast<uint16_t>(w[q] >> 16)), sc2);
     }
     const uint32_t ch = ch0 + 2 * k * CHUNK;
-    st_shared_v4(ch + sw128_chunk(row, u0), flip ? o[4] : o[0], flip ? o[5] : o[1],
-                 flip ? o[6] : o[2], flip ? o[7] : o[3]);
-    st_shared_v4(ch + sw128_chunk(row, u1), flip ? o[0] : o[4], flip ? o[1] : o[5],
-                 flip ? o[2] : o[6], flip ? o[3] : o[7]);
+    st_shared_v4(ch + sw128_chunk(row, u0), o[0], o[1], o[2], o[3]);
+    st_shared_v4(ch + sw128_chunk(row, u1), o[4], o[5], o[6], o[7]);
   }
   if (kF == FMT_V4) {  // RoPE unit j: dims 448 + 8 j .. + 8 (bf16 -> 256 x fp16), chunk 7
     const uint32_t r[4] = {c.x, c.y, c.z, c.w};
