@@ -90,7 +90,15 @@ struct TopkShared {
   uint32_t n_out, n_cand, ties, overflow, bad;
   uint32_t bin, above;       // threshold bin of the current level and the count of larger bins
   uint32_t warp_sum[32], warp_above[32];
+  uint32_t b_low;            // the sampled boundary bin (read by the peer of a CTA pair)
 };
+
+// Reads a 32-bit word of the peer CTA's shared memory (a shared::cluster address from mapa).
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 
 // Claims `take ? 1 : 0` consecutive slots of *counter for this lane with one atomic per warp;
 // returns this lane's slot (meaningful when take).
@@ -179,22 +187,27 @@ __device__ void find_threshold(TopkShared& sh, const uint32_t* hist, int nbins, 
   __syncthreads();
 }
 
-template <bool kF32>
-__global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const TopkParams p) {
+// kPair: the row is split over a cluster of two CTAs (small batches, two SMs per row): each CTA
+// takes the sampled pass and the candidate pass over half of the row's vectors (rank 1 also the
+// tail); their histograms and candidates are then merged into rank 0 through distributed
+// shared memory, and rank 0 alone runs the levels.  Both CTAs pass the same four cluster
+// barriers on every path (a row with at most k valid positions takes none).
+template <bool kF32, bool kPair>
+__device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, uint32_t* tk_smem,
+                                         int row, uint32_t rank) {
   constexpr int kKeyBits = kF32 ? 32 : 16;
   constexpr int kVec = kF32 ? 4 : 8;  // elements per 16-byte load
-  extern __shared__ uint32_t tk_smem[];
-  __shared__ TopkShared sh;
   uint32_t* hist = tk_smem;                  // [TK_BINS]
   uint32_t* cand0 = tk_smem + TK_BINS;       // [TK_CAP]
   uint32_t* cand1 = cand0 + TK_CAP;          // [TK_CAP]
-  const int row = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int req = row / p.s_q;
   int len = p.valid_len[row];
   len = len < 0 ? 0 : (len > p.ld ? p.ld : len);
   const uint8_t* rowp = static_cast<const uint8_t*>(p.scores) +
                         static_cast<size_t>(row) * p.ld * (kF32 ? 4 : 2);
   if (len <= p.k) {  // every valid position is selected
+    if (kPair && rank != 0) return;
     for (int u = tid; u < p.k; u += TK_THREADS) {
       int32_t id = -1;
       if (u < len) {
@@ -216,6 +229,10 @@ __global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const 
     sh.above = 0;
   }
   const int nvec = len / kVec;
+  // this CTA's vectors [v_lo, v_hi) and tail (the positions past the whole vectors)
+  const int v_lo = kPair && rank == 1 ? nvec / 2 : 0;
+  const int v_hi = kPair && rank == 0 ? nvec / 2 : nvec;
+  const bool own_tail = !kPair || rank == 1;
   // Sampled pass: the 12-bit histogram of every 16th vector picks a boundary bin b_low that
   // (from the sample) about 1.25 k + 256 elements reach; one full pass then keeps every element
   // of bin b_low or above as a candidate, with the exact histogram of the candidates.  The top
@@ -223,29 +240,44 @@ __global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const 
   // the buffer holds, the exact method below runs on the whole row instead.
   for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
   __syncthreads();
-  for (int v = tid * 16; v < nvec; v += TK_THREADS * 16) {
+  for (int v = v_lo + tid * 16; v < v_hi; v += TK_THREADS * 16) {
     const uint4 w = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
 #pragma unroll
     for (int e = 0; e < kVec; ++e) atomicAdd(&hist[vec_key<kF32>(w, e) >> (kKeyBits - 12)], 1u);
   }
   __syncthreads();
-  find_threshold(sh, hist, 1 << 12, static_cast<uint32_t>((5 * p.k) / 64 + 16));
-  const uint32_t b_low = sh.above + hist[sh.bin] >= static_cast<uint32_t>((5 * p.k) / 64 + 16) ? sh.bin : 0u;
+  uint32_t b_low;
+  if (kPair) {
+    cluster_sync();  // (1) both sampled histograms are complete
+    if (rank == 0) {
+      const uint32_t peer = mapa(smem_u32(hist), 1);
+      for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] += ld_peer_u32(peer + 4u * i);
+      __syncthreads();
+      find_threshold(sh, hist, 1 << 12, static_cast<uint32_t>((5 * p.k) / 64 + 16));
+      if (tid == 0)
+        sh.b_low = sh.above + hist[sh.bin] >= static_cast<uint32_t>((5 * p.k) / 64 + 16) ? sh.bin : 0u;
+    }
+    cluster_sync();  // (2) rank 0 has merged the histograms and chosen the boundary
+    b_low = rank == 0 ? sh.b_low : ld_peer_u32(mapa(smem_u32(&sh.b_low), 0));
+  } else {
+    find_threshold(sh, hist, 1 << 12, static_cast<uint32_t>((5 * p.k) / 64 + 16));
+    b_low = sh.above + hist[sh.bin] >= static_cast<uint32_t>((5 * p.k) / 64 + 16) ? sh.bin : 0u;
+  }
   __syncthreads();
   for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
   __syncthreads();
   // TK_UNROLL 16-byte loads per thread in flight, then the vectors in turn
-  for (int v0 = tid; v0 < nvec; v0 += TK_UNROLL * TK_THREADS) {
+  for (int v0 = v_lo + tid; v0 < v_hi; v0 += TK_UNROLL * TK_THREADS) {
     uint4 ws[TK_UNROLL];
 #pragma unroll
     for (int j = 0; j < TK_UNROLL; ++j) {
       const int v = v0 + j * TK_THREADS;
-      if (v < nvec) ws[j] = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
+      if (v < v_hi) ws[j] = *reinterpret_cast<const uint4*>(rowp + static_cast<size_t>(v) * 16);
     }
 #pragma unroll
     for (int j = 0; j < TK_UNROLL; ++j) {
       const int v = v0 + j * TK_THREADS;
-      if (v >= nvec) break;  // the lanes still going are a prefix of the warp
+      if (v >= v_hi) break;  // the lanes still going are a prefix of the warp
       const uint4 w = ws[j];
       uint32_t m_keep = 0;
 #pragma unroll
@@ -263,16 +295,35 @@ __global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const 
       }
     }
   }
-  for (int u = nvec * kVec + tid; u < len; u += TK_THREADS) {
-    const uint32_t key = key_at<kF32>(rowp, u);
-    const bool keep = (key >> (kKeyBits - 12)) >= b_low;
-    const uint32_t slot = warp_append(&sh.n_cand, keep);
-    if (keep) {
-      if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(u);
-      atomicAdd(&hist[key >> (kKeyBits - 12)], 1u);
+  if (own_tail) {
+    for (int u = nvec * kVec + tid; u < len; u += TK_THREADS) {
+      const uint32_t key = key_at<kF32>(rowp, u);
+      const bool keep = (key >> (kKeyBits - 12)) >= b_low;
+      const uint32_t slot = warp_append(&sh.n_cand, keep);
+      if (keep) {
+        if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(u);
+        atomicAdd(&hist[key >> (kKeyBits - 12)], 1u);
+      }
     }
   }
   __syncthreads();
+  if (kPair) {
+    cluster_sync();  // (3) both candidate passes are done
+    if (rank == 0) {  // append the peer's candidates and add its exact histogram
+      const uint32_t n0 = sh.n_cand;
+      const uint32_t n1 = ld_peer_u32(mapa(smem_u32(&sh.n_cand), 1));
+      if (n0 <= static_cast<uint32_t>(TK_CAP) && n0 + n1 <= static_cast<uint32_t>(TK_CAP)) {
+        const uint32_t pc = mapa(smem_u32(cand0), 1);
+        for (uint32_t i = tid; i < n1; i += TK_THREADS) cand0[n0 + i] = ld_peer_u32(pc + 4u * i);
+      }
+      const uint32_t ph = mapa(smem_u32(hist), 1);
+      for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] += ld_peer_u32(ph + 4u * i);
+      __syncthreads();
+      if (tid == 0) sh.n_cand = n0 + n1;  // above TK_CAP: the whole-row method below
+    }
+    cluster_sync();  // (4) rank 0 is done with the peer's shared memory
+    if (rank != 0) return;
+  }
   int src = 0;  // -1: the whole row (filtered by prefix); 0 / 1: a candidate buffer
   if (sh.n_cand < static_cast<uint32_t>(p.k) || sh.n_cand > static_cast<uint32_t>(TK_CAP)) {
     // the exact method on the whole row: the 12-bit histogram of every element
@@ -401,6 +452,22 @@ __global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const 
   if (tid == 0 && sh.bad && p.status != nullptr) atomicOr(p.status, SMLA_DEV_TOPK_TABLE);
 }
 
+template <bool kF32>
+__global__ void __launch_bounds__(TK_THREADS, SMLA_TOPK_MINB) topk_kernel(const TopkParams p) {
+  extern __shared__ uint32_t tk_smem[];
+  __shared__ TopkShared sh;
+  topk_row<kF32, false>(p, sh, tk_smem, blockIdx.x, 0);
+}
+
+// Two CTAs per row (cluster of two): small batches, where one CTA per row leaves SMs idle.
+template <bool kF32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TK_THREADS, 1)
+    topk_pair_kernel(const TopkParams p) {
+  extern __shared__ uint32_t tk_smem[];
+  __shared__ TopkShared sh;
+  topk_row<kF32, true>(p, sh, tk_smem, blockIdx.x >> 1, cluster_ctarank());
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
@@ -408,11 +475,20 @@ cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
                         int k, int ld, int max_pages, cudaStream_t stream) {
   TopkParams p{scores, valid_len, table, out, status, n_tok, s_q, k, ld, max_pages};
   const size_t smem = (TK_BINS + 2 * TK_CAP) * sizeof(uint32_t);
-  void (*kernel)(TopkParams) = fp32 ? topk_kernel<true> : topk_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // fp32 rows run on a CTA pair when the SMs outnumber the rows twice over (measured at 64
+  // rows of 32768: 20.3 -> 18.8 us; bf16 rows, half the bytes, lose more to the pair's
+  // barriers and merges than they gain: 14.7 -> 16.6 us, so they keep one CTA)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  kernel<<<n_tok, TK_THREADS, smem, stream>>>(p);
+  const bool pair = fp32 && 2 * static_cast<int64_t>(n_tok) <= sms;
+  void (*kernel)(TopkParams) = pair ? (fp32 ? topk_pair_kernel<true> : topk_pair_kernel<false>)
+                                    : (fp32 ? topk_kernel<true> : topk_kernel<false>);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kernel<<<(pair ? 2 : 1) * n_tok, TK_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

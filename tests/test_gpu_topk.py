@@ -39,10 +39,13 @@ def _check(out, scores, lens, table, s_q, k, rows=None):
         otk.check_row(out[t], sc[t], int(ln[t]), k, tb[t // s_q])
 
 
+# up to 76 rows (half the SMs) an fp32 row runs on a pair of CTAs, above that on one CTA (bf16
+# rows always on one): n_tok 12 and 96 take the two kernels
+@pytest.mark.parametrize("n_tok", [12, 96])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("ld,k", [(4096, 2048), (1000, 64), (24576, 2048), (64, 64)])
-def test_topk_parity(dev, dtype, ld, k):
-    n_tok, s_q = 12, 3
+def test_topk_parity(dev, dtype, ld, k, n_tok):
+    s_q = 3
     scores = workloads.index_scores(n_tok, ld, dtype, seed=ld + k, device=dev)
     edge = [0, 1, k - 1, k, k + 1, ld, ld + 5, -3]
     g = torch.Generator().manual_seed(k)
@@ -56,13 +59,14 @@ def test_topk_parity(dev, dtype, ld, k):
     _check(out, scores, lens, table, s_q, k)
 
 
+@pytest.mark.parametrize("n_tok", [4, 96])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("levels", [1, 3, 40])
-def test_topk_tie_heavy_rows(dev, dtype, levels):
+def test_topk_tie_heavy_rows(dev, dtype, levels, n_tok):
     # few distinct values: the threshold bin holds far more than the candidate list (8192)
-    n_tok, ld, k = 4, 40000, 2048
+    ld, k = 40000, 2048
     scores = workloads.index_scores(n_tok, ld, dtype, seed=levels, device=dev, levels=levels)
-    lens = torch.tensor([ld, ld - 7, 30000, 9000], dtype=torch.int32, device=dev)
+    lens = torch.tensor([ld, ld - 7, 30000, 9000] * (n_tok // 4), dtype=torch.int32, device=dev)
     table = _table(n_tok, (ld + 63) // 64, seed=1, dev=dev)
     out = smla.topk_page_table(scores, lens, table, 1, k)
     torch.cuda.synchronize()
