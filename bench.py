@@ -102,6 +102,15 @@ def traffic_from_profiles(kernel_src: str, profile: str, alg_bytes=None):
     return traffic
 
 
+def decode_config(spec, wl, ws: int) -> dict:
+    """The decode line's ``config``, the same for both arms (the workload, not how it is
+    timed: the reference arm's token sample is in its ``cpu_baseline.sample``)."""
+    return {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
+            "topk": spec.topk, "ctx": spec.ctx, "num_blocks": int(wl.kv.shape[0]),
+            "valid_slots": int(wl.num_valid),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU", "l2": FLUSH_NOTE}
+
+
 def traffic_from_pair_profile(sources, profile: str):
     """DRAM bytes per step of a chain of kernels from one committed ncu summary that lists a
     ``code_sha256 <file>: <hash>`` line per kernel source and their summed
@@ -395,9 +404,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
-                   "topk": spec.topk, "ctx": spec.ctx,
-                   "sample": f"first {per_step_tokens} query tokens per step"},
+        "config": decode_config(spec, wl, ws),
         "gathered_tokens_per_s": valid / total,
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": oracle.max_threads(),
                          "kind": "oracle",
@@ -758,10 +765,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
-            "config": {"workload": spec.name, "b": spec.b, "s_q": spec.s_q, "h_q": spec.h_q,
-                       "topk": spec.topk, "ctx": spec.ctx, "num_blocks": int(wl.kv.shape[0]),
-                       "valid_slots": nvalid, "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
-                       "l2": FLUSH_NOTE},
+            "config": decode_config(spec, wl, ws),
             "gathered_tokens_per_s": ws * nvalid / t_step,
             "tflops_all_slots": ws * flops_all / t_step / 1e12,
             "kernel_ms": {"decode": statistics.mean(dec_ms),

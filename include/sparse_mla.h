@@ -173,7 +173,11 @@ smla_status sparse_mla_sched_meta(const smla_dims* dims, int num_sms, void* sche
  *              row with no valid slot
  * Asynchronous on stream.  Errors: SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED,
  * SMLA_ERR_ALIGNMENT, SMLA_ERR_WORKSPACE, SMLA_ERR_CUDA.  Device-side problems (a wait
- * that ran out, q or a scale outside the fp16 range) set bits of the status word.
+ * that ran out, q or a scale outside the fp16 range) set bits of the status word.  The
+ * kernels compute in fp16: q with |q| > 65504, a scale whose product with 256 leaves the
+ * fp16 normal range, or a dequantized key beyond 65504 / 256 are UNSUPPORTED inputs, not
+ * merely reported ones: out and lse are then not valid (SMLA_DEV_Q_RANGE,
+ * SMLA_DEV_SCALE_RANGE or SMLA_DEV_NAN_INPUT tells the caller after the fact).
  */
 smla_status sparse_mla_decode_fwd(const smla_dims* dims, int num_sms, const void* q,
                                   const void* kv_cache, const int32_t* indices, float sm_scale,

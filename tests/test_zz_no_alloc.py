@@ -17,7 +17,8 @@ from tests.gpu_util import compare, gpu_tokens
 
 def _static_run(wl, num_sms):
     import torch
-    d = smla.dims_for(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk, wl.kv.shape[0])
+    d = smla.dims_for(wl.spec.b, wl.spec.s_q, wl.spec.h_q, wl.spec.topk, wl.kv.shape[0],
+                      kv_format=wl.spec.kv_format)
     out = torch.empty(wl.spec.b, wl.spec.s_q, wl.spec.h_q, 512, dtype=torch.bfloat16,
                       device=wl.q.device)
     lse = torch.empty(wl.spec.b, wl.spec.h_q, wl.spec.s_q, dtype=torch.float32, device=wl.q.device)
@@ -128,3 +129,22 @@ def test_static_survives_a_device_reset(cuda_ok):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     assert "STATIC RESET CHILD OK" in r.stdout
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["v41", "v4"])
+def test_static_runs_the_later_formats(cuda_ok, fmt):
+    # the static scratch takes any problem that fits, whatever the cache format
+    import torch
+    from tests.gpu_util import run_cuda
+    smla.lib()
+    dev = torch.device("cuda:0")
+    wl = workloads.small(b=3, s_q=2, h_q=128, topk=300, ctx=2048, masked_per_row=5, seed=57,
+                         device=dev, kv_format=fmt)
+    out_r, lse_r, _ = run_cuda(wl, num_sms=152)
+    out_s, lse_s = _static_run(wl, 152)
+    torch.cuda.synchronize()
+    assert torch.equal(out_s, out_r) and torch.equal(lse_s, lse_r)
+    d = smla.dims_for(3, 2, 128, 300, wl.kv.shape[0], kv_format=fmt)
+    rc, word = smla.sparse_mla_static_read_status(d, 152)
+    assert rc == smla.SMLA_OK and word == 0
