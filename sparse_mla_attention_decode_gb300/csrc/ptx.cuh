@@ -68,9 +68,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // ------------------------------------------------------------------ tiled tensor copy (TMA)
 // One box of a 2-D tensor map (in kernel-parameter space) into this CTA's shared memory,
@@ -114,15 +111,6 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// ------------------------------------------------------------------ bulk copy (global -> smem)
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Bulk copy from this CTA's shared memory into a peer CTA's shared memory; completes bytes on
 // the peer's mbarrier (dst and bar are shared::cluster addresses of the peer).
 __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
@@ -148,26 +136,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-// 16-byte asynchronous store into a peer CTA's shared memory; completes bytes on the peer's
-// mbarrier (both addresses are shared::cluster addresses of the peer).
-__device__ __forceinline__ void st_async_v4(uint32_t dst, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
-      : "memory");
-}
-
-// ------------------------------------------------------------------ register reallocation
-// All warps of a warpgroup execute these together (warp-group-wide .sync.aligned).
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 // ------------------------------------------------------------------ PDL
 __device__ __forceinline__ void griddep_wait() {
@@ -190,15 +158,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // D[tmem] (+)= A[smem desc] * B[smem desc] with e4m3 A and B (kind::f8f6f4; K = 32 per MMA).
 __device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -206,15 +165,6 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, ui
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Warp-collective forms: every lane of a converged warp executes the instruction and
@@ -313,12 +263,9 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, int b_mn_maj
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// Byte offset of 16-bit element (row, k) inside a [rows x 64] K-major tile with the 128-byte
-// swizzle (tile base 1024-byte aligned): 8-row atoms of 1024 bytes, 16-byte chunks XOR row%8.
-__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t k) {
-  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((k >> 3) ^ row) & 7u) << 4) + (k & 7u) * 2u;
-}
-// Byte offset of the 16-byte chunk c (8 elements) of row `row` in the same layout.
+// Byte offset of the 16-byte chunk c (8 16-bit elements) of row `row` inside a [rows x 64]
+// K-major tile with the 128-byte swizzle (tile base 1024-byte aligned): 8-row atoms of 1024
+// bytes, 16-byte chunks XOR row%8.
 __device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t c) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + (((c ^ row) & 7u) << 4);
 }
@@ -382,11 +329,6 @@ __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
 }
 __device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t& a, uint32_t& b) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
 }
 __device__ __forceinline__ int32_t ldg_s32(const int32_t* p) {
   int32_t v;
