@@ -111,6 +111,12 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Starts fetching `bytes` of global memory (a multiple of 16, from a 16-byte aligned address)
+// into L2 without waiting for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Bulk copy from this CTA's shared memory into a peer CTA's shared memory; completes bytes on
 // the peer's mbarrier (dst and bar are shared::cluster addresses of the peer).
 __device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, uint32_t src, uint32_t bytes,

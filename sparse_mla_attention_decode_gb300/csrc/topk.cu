@@ -43,7 +43,8 @@ namespace {
 #define SMLA_TOPK_MINB 2
 #endif
 constexpr int TK_THREADS = SMLA_TOPK_THREADS;
-constexpr int TK_CAP = SMLA_TOPK_CAP;         // candidate positions per buffer (two buffers)
+constexpr int TK_CAP = SMLA_TOPK_CAP;         // candidate positions of the first buffer
+constexpr int TK_CAP1 = TK_CAP / 2;           // of the second (the later levels keep fewer)
 constexpr int TK_UNROLL = SMLA_TOPK_UNROLL;   // 16-byte loads per thread in flight
 constexpr int TK_BINS = 4096;  // the widest level (12 bits)
 
@@ -84,6 +85,33 @@ __device__ __forceinline__ uint32_t vec_key(const uint4& w, int e) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   if (kF32) return to_key<true>(ws[e]);
   return to_key<false>((ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+}
+
+// Bit e set when element e of a 16-byte vector has a key of at least t (the full-width key of
+// the sampled boundary).  Keys grow with the score, so when t lies in the upper half of the key
+// range (a non-negative threshold) an element qualifies exactly when its bits, read as a signed
+// integer, are at least t - 2^(n-1): negative scores never do.  `a` is that bound, for bf16
+// shifted into the upper 16 bits (a bf16 in the upper half of a word is compared as the whole
+// word, one in the lower half after a shift).  Other thresholds compare the keys.
+template <bool kF32>
+__device__ __forceinline__ uint32_t keep_mask(const uint4& w, bool fast, int32_t a, uint32_t t) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  uint32_t m = 0;
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (kF32) {
+        m |= static_cast<uint32_t>(static_cast<int32_t>(ws[i]) >= a) << i;
+      } else {
+        m |= static_cast<uint32_t>(static_cast<int32_t>(ws[i] << 16) >= a) << (2 * i);
+        m |= static_cast<uint32_t>(static_cast<int32_t>(ws[i]) >= a) << (2 * i + 1);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < (kF32 ? 4 : 8); ++e) m |= static_cast<uint32_t>(vec_key<kF32>(w, e) >= t) << e;
+  }
+  return m;
 }
 
 struct TopkShared {
@@ -199,7 +227,8 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
   constexpr int kVec = kF32 ? 4 : 8;  // elements per 16-byte load
   uint32_t* hist = tk_smem;                  // [TK_BINS]
   uint32_t* cand0 = tk_smem + TK_BINS;       // [TK_CAP]
-  uint32_t* cand1 = cand0 + TK_CAP;          // [TK_CAP]
+  uint32_t* ckey0 = cand0 + TK_CAP;          // [TK_CAP] keys of the first candidates
+  uint32_t* cand1 = ckey0 + TK_CAP;          // [TK_CAP1]
   const int tid = threadIdx.x;
   const int req = row / p.s_q;
   int len = p.valid_len[row];
@@ -238,6 +267,14 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
   // of bin b_low or above as a candidate, with the exact histogram of the candidates.  The top
   // k are all among the candidates when there are at least k of them; with fewer, or more than
   // the buffer holds, the exact method below runs on the whole row instead.
+  // the CTA's part of the row on its way into L2 (16 KB per request) while the sampled pass
+  // runs, so that the full pass reads it from L2
+  {
+    const uint32_t bytes = static_cast<uint32_t>(v_hi - v_lo) * 16u;
+    for (uint32_t c = static_cast<uint32_t>(tid); c * 16384u < bytes; c += TK_THREADS)
+      bulk_prefetch_l2(rowp + static_cast<size_t>(v_lo) * 16 + c * 16384u,
+                       bytes - c * 16384u < 16384u ? bytes - c * 16384u : 16384u);
+  }
   for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
   __syncthreads();
   for (int v = v_lo + tid * 16; v < v_hi; v += TK_THREADS * 16) {
@@ -266,6 +303,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
   __syncthreads();
   for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] = 0;
   __syncthreads();
+  // the candidate test as a compare on the raw bits when the boundary is non-negative
+  const uint32_t t_low = b_low << (kKeyBits - 12);
+  const bool fast = t_low >= (1u << (kKeyBits - 1));
+  const int32_t a_fast = static_cast<int32_t>((t_low - (1u << (kKeyBits - 1))) << (32 - kKeyBits));
   // TK_UNROLL 16-byte loads per thread in flight, then the vectors in turn
   for (int v0 = v_lo + tid; v0 < v_hi; v0 += TK_UNROLL * TK_THREADS) {
     uint4 ws[TK_UNROLL];
@@ -279,19 +320,20 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
       const int v = v0 + j * TK_THREADS;
       if (v >= v_hi) break;  // the lanes still going are a prefix of the warp
       const uint4 w = ws[j];
-      uint32_t m_keep = 0;
-#pragma unroll
-      for (int e = 0; e < kVec; ++e)
-        m_keep |= static_cast<uint32_t>((vec_key<kF32>(w, e) >> (kKeyBits - 12)) >= b_low) << e;
+      uint32_t m_keep = keep_mask<kF32>(w, fast, a_fast, t_low);
       const unsigned mask = __activemask();
       if (!__any_sync(mask, m_keep != 0u)) continue;
       uint32_t slot = warp_reserve(&sh.n_cand, __popc(m_keep));
       while (m_keep) {
         const int e = __ffs(m_keep) - 1;
         m_keep &= m_keep - 1u;
-        if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(v * kVec + e);
+        const uint32_t key = vec_key<kF32>(w, e);
+        if (slot < TK_CAP) {
+          cand0[slot] = static_cast<uint32_t>(v * kVec + e);
+          ckey0[slot] = key;
+        }
         ++slot;
-        atomicAdd(&hist[vec_key<kF32>(w, e) >> (kKeyBits - 12)], 1u);
+        atomicAdd(&hist[key >> (kKeyBits - 12)], 1u);
       }
     }
   }
@@ -301,7 +343,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
       const bool keep = (key >> (kKeyBits - 12)) >= b_low;
       const uint32_t slot = warp_append(&sh.n_cand, keep);
       if (keep) {
-        if (slot < TK_CAP) cand0[slot] = static_cast<uint32_t>(u);
+        if (slot < TK_CAP) {
+          cand0[slot] = static_cast<uint32_t>(u);
+          ckey0[slot] = key;
+        }
         atomicAdd(&hist[key >> (kKeyBits - 12)], 1u);
       }
     }
@@ -314,7 +359,11 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
       const uint32_t n1 = ld_peer_u32(mapa(smem_u32(&sh.n_cand), 1));
       if (n0 <= static_cast<uint32_t>(TK_CAP) && n0 + n1 <= static_cast<uint32_t>(TK_CAP)) {
         const uint32_t pc = mapa(smem_u32(cand0), 1);
-        for (uint32_t i = tid; i < n1; i += TK_THREADS) cand0[n0 + i] = ld_peer_u32(pc + 4u * i);
+        const uint32_t pk = mapa(smem_u32(ckey0), 1);
+        for (uint32_t i = tid; i < n1; i += TK_THREADS) {
+          cand0[n0 + i] = ld_peer_u32(pc + 4u * i);
+          ckey0[n0 + i] = ld_peer_u32(pk + 4u * i);
+        }
       }
       const uint32_t ph = mapa(smem_u32(hist), 1);
       for (int i = tid; i < TK_BINS; i += TK_THREADS) hist[i] += ld_peer_u32(ph + 4u * i);
@@ -359,7 +408,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
       for (int i = tid; i < (1 << nbits); i += TK_THREADS) hist[i] = 0;
     __syncthreads();
     uint32_t* dst = src == 0 ? cand1 : cand0;
+    const uint32_t dcap = src == 0 ? static_cast<uint32_t>(TK_CAP1) : static_cast<uint32_t>(TK_CAP);
     const uint32_t* srcb = src == 0 ? cand0 : cand1;
+    // the first candidates carry their keys (the later buffers hold positions only)
+    const bool src_keys = src == 0 && level == 0;
     // one element: emit it (larger bin, or bin b when all of it or, at the last level, a tie
     // within the count), or keep it as a candidate of the next level
     auto visit = [&](bool in, int u, uint32_t key) {
@@ -382,7 +434,7 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
       if (!last && !all_of_bin) {
         const uint32_t slot = warp_append(&sh.n_cand, keep);
         if (keep) {
-          if (slot < TK_CAP) dst[slot] = static_cast<uint32_t>(u);
+          if (slot < dcap) dst[slot] = static_cast<uint32_t>(u);
           else sh.overflow = 1u;
           atomicAdd(&hist[(key >> (shift - nbits)) & ((1u << nbits) - 1u)], 1u);
         }
@@ -413,7 +465,7 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
         while (m_keep) {
           const int e = __ffs(m_keep) - 1;
           m_keep &= m_keep - 1u;
-          if (slot < TK_CAP) dst[slot] = static_cast<uint32_t>(v * kVec + e);
+          if (slot < dcap) dst[slot] = static_cast<uint32_t>(v * kVec + e);
           else sh.overflow = 1u;
           ++slot;
           atomicAdd(&hist[(vec_key<kF32>(w, e) >> (shift - nbits)) & ((1u << nbits) - 1u)], 1u);
@@ -438,7 +490,7 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, TopkShared& sh, ui
     } else {
       for (uint32_t i = tid; i < n_src; i += TK_THREADS) {
         const int u = static_cast<int>(srcb[i]);
-        visit(true, u, key_at<kF32>(rowp, u));
+        visit(true, u, src_keys ? ckey0[i] : key_at<kF32>(rowp, u));
       }
     }
     __syncthreads();
@@ -474,7 +526,7 @@ cudaError_t launch_topk(const void* scores, bool fp32, const int32_t* valid_len,
                         const int32_t* table, int32_t* out, uint32_t* status, int n_tok, int s_q,
                         int k, int ld, int max_pages, cudaStream_t stream) {
   TopkParams p{scores, valid_len, table, out, status, n_tok, s_q, k, ld, max_pages};
-  const size_t smem = (TK_BINS + 2 * TK_CAP) * sizeof(uint32_t);
+  const size_t smem = (TK_BINS + 2 * TK_CAP + TK_CAP1) * sizeof(uint32_t);
   // fp32 rows run on a CTA pair when the SMs outnumber the rows twice over (measured at 64
   // rows of 32768: 20.3 -> 18.8 us; bf16 rows, half the bytes, lose more to the pair's
   // barriers and merges than they gain: 14.7 -> 16.6 us, so they keep one CTA)
