@@ -471,30 +471,38 @@ def run_topk(args):
 
 
 def run_indexer(args):
-    """The lightning-indexer scores on the decode workload's shape: 64 requests, one query token
-    each, over 32768 cached tokens (512 indexer pages of 8448 bytes) per request.  HBM-bound: the
-    algorithmic bytes are the key pages read once per request (132 bytes a token), the fp32
-    scores written and the e4m3 Q and fp32 weights read.  L2 is flushed between steps (the
-    277 MB of pages are larger than L2 too)."""
+    """The lightning-indexer scores.  --indexer-shape decode (default): 64 requests, one query
+    token each, over 32768 cached tokens (512 indexer pages of 8448 bytes) per request;
+    HBM-bound: the algorithmic bytes are the key pages read once per request (132 bytes a
+    token), the fp32 scores written and the e4m3 Q and fp32 weights read.  L2 is flushed
+    between steps (the 277 MB of pages are larger than L2 too).  --indexer-shape prefill: one
+    request, 4096 query tokens over a 65536-token cache, causal (query i sees positions
+    [0, 61441 + i]); tensor-bound (2 * 64 * 128 flop per query token and visible position,
+    e4m3 MMAs), against the FP8 dense peak taken as twice the measured bf16 one."""
     import torch
 
     import sparse_mla_attention_decode_gb300 as smla
     import workloads
 
     dev = torch.device("cuda:0")
-    b, ctx = 64, 32768
+    prefill = args.indexer_shape == "prefill"
+    b, s_q, ctx = (1, 4096, 65536) if prefill else (64, 1, 32768)
+    n_tok = b * s_q
     pages = ctx // 64
     cache = workloads.indexer_cache(b * pages, seed=1, device=dev)
-    q8, w = workloads.indexer_queries(b, seed=2, device=dev)
+    q8, w = workloads.indexer_queries(n_tok, seed=2, device=dev)
     table = torch.randperm(b * pages, generator=torch.Generator().manual_seed(3))
     table = table.to(torch.int32).view(b, pages).to(dev)
-    lens = torch.full((b,), ctx, dtype=torch.int32, device=dev)
-    out = torch.empty(b, ctx, dtype=torch.float32, device=dev)
+    if prefill:
+        lens = (61441 + torch.arange(n_tok, device=dev)).clamp(max=ctx).to(torch.int32)
+    else:
+        lens = torch.full((n_tok,), ctx, dtype=torch.int32, device=dev)
+    out = torch.empty(n_tok, ctx, dtype=torch.float32, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         flush()
-        smla.indexer_scores(q8, w, cache, table, lens, 1, ctx, out=out)
+        smla.indexer_scores(q8, w, cache, table, lens, s_q, ctx, out=out)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(0)
     sampler.start()
@@ -504,30 +512,49 @@ def run_indexer(args):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        smla.indexer_scores(q8, w, cache, table, lens, 1, ctx, out=out)
+        smla.indexer_scores(q8, w, cache, table, lens, s_q, ctx, out=out)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ts.append(e0.elapsed_time(e1) / 1e3)
     clocks = sampler.stop()
     t = sum(ts) / len(ts)
-    alg = b * ctx * 132 + b * ctx * 4 + b * (64 * 128 + 64 * 4)
-    flops = 2.0 * 64 * 128 * b * ctx
+    visible = int(lens.sum().item())
+    # the pages of a request are read once (its query tokens share them)
+    req_len = int(lens.view(b, s_q).max(dim=1).values.sum().item())
+    alg = req_len * 132 + visible * 4 + n_tok * (64 * 128 + 64 * 4)
+    flops = 2.0 * 64 * 128 * visible
     peaks, peak_src = load_peaks()
-    peak = float(peaks["hbm_gbs"])
-    achieved = alg / t / 1e9
-    traffic = traffic_from_profiles(os.path.join(CSRC, "indexer.cu"),
-                                    f"indexer_kernel_decode_b{b}_ctx{ctx}.md", alg)
+    workload = f"indexer_prefill_sq{s_q}_ctx{ctx}" if prefill else f"indexer_decode_b{b}_ctx{ctx}"
+    config = {"workload": workload, "requests": b, "query_tokens": n_tok, "ctx": ctx,
+              "heads": 64, "dim": 128, "l2": FLUSH_NOTE}
+    if prefill:
+        config["causal_base"] = 61441
+        peak = 2.0 * float(peaks["bf16_tflops"])
+        achieved = flops / t / 1e12
+        metric = ("lightning-indexer scores (e4m3 tensor-core MMA + ReLU + weighted head sum), "
+                  "TFLOP/s")
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "peak_kind": f"2 x the {peak_src} bf16 burst (FP8 dense = 2 x bf16 nominal)",
+                    "alg_bytes_per_launch": alg}
+        value, unit = achieved, "TFLOP/s"
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = alg / t / 1e9
+        traffic = traffic_from_profiles(os.path.join(CSRC, "indexer.cu"),
+                                        f"indexer_kernel_decode_b{b}_ctx{ctx}.md", alg)
+        metric = ("lightning-indexer scores (e4m3 tensor-core MMA + ReLU + weighted head sum), "
+                  "bytes/s")
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "peak_kind": f"{peak_src} copy bandwidth", "alg_bytes_per_launch": alg}
+        value, unit = achieved, "GB/s"
     print(json.dumps({
-        "metric": "lightning-indexer scores (e4m3 tensor-core MMA + ReLU + weighted head sum), "
-                  "bytes/s", "impl": "gb300", "value": achieved, "unit": "GB/s", "n_gpus": 1,
+        "metric": metric, "impl": "gb300", "value": value, "unit": unit, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
-        "config": {"workload": f"indexer_decode_b{b}_ctx{ctx}", "requests": b, "ctx": ctx,
-                   "heads": 64, "dim": 128, "l2": FLUSH_NOTE},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_kind": f"{peak_src} copy bandwidth", "alg_bytes_per_launch": alg},
-        "tflops": flops / t / 1e12, "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+        "config": config, "roofline": roofline, "tflops": flops / t / 1e12,
+        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
 
 def run_select(args):
@@ -615,6 +642,9 @@ def main():
                          "selection with the page-table emit; indexer: the indexer scores; "
                          "select: the two chained; each on its own line")
     ap.add_argument("--topk-rows", type=int, default=4096)
+    ap.add_argument("--indexer-shape", default="decode", choices=["decode", "prefill"],
+                    help="--kernel indexer: the decode shape (64 requests x 32768, HBM-bound) or "
+                         "the prefill shape (4096 query tokens x 65536, tensor-bound)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
