@@ -533,8 +533,10 @@ def run_indexer(args):
         achieved = flops / t / 1e12
         metric = ("lightning-indexer scores (e4m3 tensor-core MMA + ReLU + weighted head sum), "
                   "TFLOP/s")
+        traffic = traffic_from_profiles(os.path.join(CSRC, "indexer.cu"),
+                                        f"indexer_kernel_prefill_sq{s_q}_ctx{ctx}.md", alg)
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": None,
+                    "frac": achieved / peak, "traffic": traffic,
                     "peak_kind": f"2 x the {peak_src} bf16 burst (FP8 dense = 2 x bf16 nominal)",
                     "alg_bytes_per_launch": alg}
         value, unit = achieved, "TFLOP/s"

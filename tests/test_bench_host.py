@@ -52,7 +52,8 @@ def test_committed_profiles_match_the_current_kernels():
                       ("decode_fwd.cu", "decode_kernel_c5_b1_sq4096_h128_k2048.md"),
                       ("decode_fwd.cu", "decode_kernel_c4_b32_h128_k2048_ue8m0_sorted.md"),
                       ("topk.cu", "topk_kernel_prefill_1024x65536_k2048.md"),
-                      ("indexer.cu", "indexer_kernel_decode_b64_ctx32768.md")):
+                      ("indexer.cu", "indexer_kernel_decode_b64_ctx32768.md"),
+                      ("indexer.cu", "indexer_kernel_prefill_sq4096_ctx65536.md")):
         assert bench.traffic_from_profiles(os.path.join(csrc, src), prof) is not None, prof
     # the selection chain's two kernels share one summary
     assert bench.traffic_from_pair_profile(
