@@ -670,17 +670,23 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
 // max), not per converted value: the conversion is issue-bound on the SM sub-partitions.
 // False if a wait ran out.
 static_assert(9 * 128 * 128 <= OFF_MSG, "Q fits in the key-tile region");
+// The copies alone (one thread).  For a cluster's later items they are issued as soon as the
+// QK of the current item's last block has completed (the region and Q's tensor-memory columns
+// are free from then on), so that they land while that block's softmax runs.
+__device__ void issue_q(const DecodeParams& p, const Ctx& c, int tok) {
+  const uint32_t qs = c.sbase + OFF_TILE;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
+  for (int ch = 0; ch < p.q_chunks; ++ch) {
+    mbar_arrive_expect_tx(c.bar(B_QLOAD + ch), chunk_bytes);
+    tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD + ch));
+  }
+}
 __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, int tok, int i,
-                             uint32_t& bad, uint32_t item) {
+                             uint32_t& bad, uint32_t item, bool issued = false) {
   const uint32_t qs = c.sbase + OFF_TILE;
   const uint32_t chunk_bytes = static_cast<uint32_t>(p.h_q) * 128;
   const int nch = p.q_chunks;
-  if (i == 0) {
-    for (int ch = 0; ch < nch; ++ch) {
-      mbar_arrive_expect_tx(c.bar(B_QLOAD + ch), chunk_bytes);
-      tma_load_2d(qs + ch * chunk_bytes, &p.q_map, ch * 64, tok * p.h_q, c.bar(B_QLOAD + ch));
-    }
-  }
+  if (i == 0 && !issued) issue_q(p, c, tok);
   const bool live = i < p.h_q;
   const uint32_t row = qs + static_cast<uint32_t>(i) * 128;
   const uint32_t sw = static_cast<uint32_t>(i & 7);
@@ -779,6 +785,12 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       const uint32_t sb = g % NSBUF, st = g % NMSG;
       if (!c.wait_warp(B_S_FULL + sb, (g / NSBUF) & 1)) goto out;
       tc_fence_after();
+      // the item's last QK has completed: the next item's Q copies can start now
+      if (i == 0 && blk == b1 - 1 && !pl.last_item(s, req)) {
+        const int nreq = req < pl.end_req ? req + 1 : pl.begin_req;
+        const int ns = req < pl.end_req ? s : s + pl.s_step;
+        issue_q(p, c, nreq * p.s_q + ns);
+      }
       // the block's validity bits, copied into tensor memory with its QK (the same commit)
       uint32_t mk[2];
       tmem_ld2(tbase + lane_base + TM_M + 4 * (g % NVMASK), mk);
@@ -850,12 +862,13 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
         bulk_s2s_cluster(peer_msg + st * MSG_STRIDE, msg, MSG_BYTES, peer_full + st * 8);
       }
     }
-    // every QK^T of this range has completed: stage the next item's Q (the next request at
-    // this position, else the first request at the cluster's next position)
+    // every QK^T of this range has completed: convert the next item's Q (the next request at
+    // this position, else the first request at the cluster's next position), whose copies
+    // were issued when the range's last QK completed
     if (!pl.last_item(s, req)) {
       const int nreq = req < pl.end_req ? req + 1 : pl.begin_req;
       const int ns = req < pl.end_req ? s : s + pl.s_step;
-      if (!stage_q_bulk(p, c, tq, nreq * p.s_q + ns, i, qbad, item + 1)) goto out;
+      if (!stage_q_bulk(p, c, tq, nreq * p.s_q + ns, i, qbad, item + 1, true)) goto out;
     }
   }
 out:
