@@ -14,11 +14,12 @@
 //
 // Work item = (query group of G <= 4 tokens of one request, chunk of 16 key tiles); each CTA
 // takes an equal contiguous range of the key tiles of all groups laid end to end, so
-// consecutive items share their group's Q.  Warps 0-7: epilogue, two warpgroups (thread =
-// TMEM lane = token) taking alternate (tile, query token) units; warp 8: TMA producer (Q once
-// per run of items of one group into one of two buffers; per key tile the two pages' codes
-// and their key scales, as many stages as fit beside Q); warp 9: MMA issuer (TMEM
-// accumulators of 64 G columns: eight at G = 1, four at G = 2, two above).  A stage is
+// consecutive items share their group's Q.  The first 4 NG warps: epilogue, NG warpgroups
+// (thread = TMEM lane = token; NG = 2 at one query token per group, 3 above) taking the (tile,
+// query token) units in turn; then the TMA producer (Q once per run of items of one group into
+// one of two buffers; per key tile the two pages' codes and their key scales, as many stages
+// as fit beside Q) and the MMA issuer (TMEM accumulators of 64 G columns: eight at G = 1,
+// four at G = 2, two above).  A stage is
 // released by the epilogue once it has read the tile's key scales (the MMAs are done by then),
 // and the page ids, lengths and head weights of the next item load while the current one
 // runs, so no global load sits on a role's critical path.  Every wait is bounded (a second),
@@ -32,7 +33,14 @@
 namespace smla {
 namespace {
 
-constexpr int IX_THREADS = 320;  // warps 0-7 epilogue, 8 TMA producer, 9 MMA issuer
+// Warps [0, 4 NG): epilogue (NG warpgroups), 4 NG: TMA producer, 4 NG + 1: MMA issuer.  NG = 2
+// at one query token per group, 3 when a group has several (the epilogue then sets the pace,
+// and a third warpgroup hides more of its latency).
+template <int NG>
+struct IxWarps {
+  static constexpr int kEpi = 4 * NG, kProducer = 4 * NG, kMma = 4 * NG + 1;
+  static constexpr int kThreads = 32 * (4 * NG + 2);
+};
 constexpr int IX_MAX_STAGES = 12;
 constexpr int IX_TILE = 128;          // cached tokens per key tile (two pages)
 constexpr int IX_PAGE_BYTES = 8448;   // 64 x 128 codes + 64 x 4 scale bytes
@@ -49,16 +57,18 @@ enum IxBar {
   IB_NEVER,                                 // nothing arrives (the failure-path test)
   IB_COUNT
 };
-// Shared memory (base 1024-aligned): barriers, [8 warps][256] head weights (read as float4),
-// TMEM slot + abort flag, then the stages (codes, 16 KB each, 1024-aligned for the 128-byte
-// swizzle), their key scales, and two Q buffers of 64 G x 128 bytes.  The number of stages
-// is what fits beside the Q buffers: 12 at G = 1, 11, 10, 9 at G = 4.
+// Shared memory (base 1024-aligned): barriers, [epilogue warps][256] head weights (read as
+// float4), TMEM slot + abort flag, then the stages (codes, 16 KB each, 1024-aligned for the
+// 128-byte swizzle), their key scales, and two Q buffers of 64 G x 128 bytes.  The number of
+// stages is what fits beside the Q buffers: 12 at G = 1, 10, 9, 8 at G = 4.
 constexpr int IX_OFF_BARS = 0;
 constexpr int IX_OFF_W = 512;
 static_assert(IB_COUNT * 8 <= IX_OFF_W, "barriers fit below the weights");
-constexpr int IX_OFF_MISC = IX_OFF_W + 8 * 256 * 4;
-constexpr int IX_OFF_STAGES = 9 * 1024;
-static_assert(IX_OFF_MISC + 32 <= IX_OFF_STAGES, "fixed part fits below the stages");
+template <int NG>
+struct IxLayout {
+  static constexpr int kOffMisc = IX_OFF_W + IxWarps<NG>::kEpi * 256 * 4;
+  static constexpr int kOffStages = (kOffMisc + 32 + 1023) / 1024 * 1024;
+};
 constexpr int IX_SMEM_MAX = 227 * 1024;
 constexpr uint64_t kIxWaitNs = 1000000000ull;
 
@@ -77,7 +87,8 @@ struct IndexerParams {
   int max_tiles;  // key tiles of a full row (ld / 128, rounded up)
   int nshift;  // 1 << nshift TMEM accumulators of 512 >> nshift columns
   int stages;  // key-tile stages
-  uint32_t off_sc, off_q, q_bytes;  // shared-memory offsets of the scales and Q buffers
+  uint32_t off_stages, off_sc, off_q, q_bytes;  // shared-memory offsets of the stages, their
+                                                // scales and the Q buffers
   int test_stall;                   // the MMA issuer waits on IB_NEVER (bounded) and leaves
   int64_t num_pages;
 };
@@ -250,7 +261,7 @@ __device__ void ix_producer(const IndexerParams& p, const IxCtx& c, int lane) {
         if (lane == 0) {
           ok = (gt < static_cast<uint32_t>(p.stages) || c.wait(IB_K_EMPTY + st, ph ^ 1u)) ? 1 : 0;
           if (ok) {
-            const uint32_t dst = c.sbase + IX_OFF_STAGES + st * IX_STAGE_BYTES;
+            const uint32_t dst = c.sbase + p.off_stages + st * IX_STAGE_BYTES;
             const uint32_t sdst = c.sbase + p.off_sc + st * IX_SC_BYTES;
             // a page id outside [0, num_pages) reads the fill value: zero codes and scales
             mbar_arrive_expect_tx(c.bar(IB_K_FULL + st), IX_STAGE_BYTES + IX_SC_BYTES);
@@ -314,7 +325,7 @@ __device__ void ix_mma(const IndexerParams& p, const IxCtx& c, uint32_t tbase) {
       if (!c.wait(IB_K_FULL + st, ph)) return;
       if (gt >= nbuf && !c.wait(IB_D_EMPTY + db, ((gt >> p.nshift) - 1) & 1)) return;
       tc_fence_after();
-      const uint64_t adesc = umma_desc(c.sbase + IX_OFF_STAGES + st * IX_STAGE_BYTES, 16, 1024, 2);
+      const uint64_t adesc = umma_desc(c.sbase + p.off_stages + st * IX_STAGE_BYTES, 16, 1024, 2);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // 32 codes = 32 bytes of each row per MMA
         mma_ss_f8(tbase + db * colw, adesc + (kk * 32 >> 4), bdesc + (kk * 32 >> 4), idesc, kk > 0);
@@ -327,12 +338,14 @@ __device__ void ix_mma(const IndexerParams& p, const IxCtx& c, uint32_t tbase) {
   }
 }
 
-// Epilogue warpgroup `grp` (0: warps 0-3, 1: warps 4-7; thread i = TMEM lane = cached token)
-// takes every other (key tile, query token) unit of the item, unit = tile * gs + q, so that
-// both warpgroups work at every group size (alternate tiles for one query token).  Each warp stages the item's head
-// weights in its own shared-memory slice (no barrier beyond the warp) and reads them four at a
-// time; a token's 64 accumulator columns are loaded before one wait.  The key scale comes from
-// the stage (loaded with the codes); the warp releases the stage once it has read it.
+// Epilogue warpgroup `grp` of NG (warps 4 grp .. 4 grp + 3; thread i = TMEM lane = cached
+// token) takes the units u = (tile - base) * gs + q of the item with u % NG == grp, so that
+// every warpgroup works at every group size (tiles in turn for one query token).  Each warp
+// stages the item's head weights in its own shared-memory slice (no barrier beyond the warp)
+// and reads them four at a time; a token's 64 accumulator columns are loaded and weighed in
+// two halves of 32.  The key scale comes from the stage (loaded with the codes); the warp
+// releases the stage once it has read it.
+template <int NG>
 __device__ void ix_epilogue(const IndexerParams& p, const IxCtx& c, uint32_t tbase, int i,
                             int grp, float* wsm, const float* scales) {
   const uint32_t lane_base = static_cast<uint32_t>((i >> 5) * 32) << 16;
@@ -395,25 +408,30 @@ __device__ void ix_epilogue(const IndexerParams& p, const IxCtx& c, uint32_t tba
         ph ^= 1u;
       }
       const int s = tile * IX_TILE + i;  // this thread's cached token
-      const int q_first = (grp + (tile - it.base) * it.gs) & 1;
+      // this warpgroup's units of the tile: the query tokens q with ((tile - base) gs + q) %
+      // NG == grp; a token's 64 columns are weighed in two halves of 32
+      const int q_first = ((grp - ((tile - it.base) * it.gs) % NG) + NG) % NG;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int q = q_first + 2 * k;
+      for (int k = 0; k < (4 + NG - 1) / NG; ++k) {
+        const int q = q_first + NG * k;
         if (q >= it.gs) break;
         const int nq = q == 0 ? nq0 : (q == 1 ? nq1 : (q == 2 ? nq2 : nq3));
-        uint32_t r[64];
-#pragma unroll
-        for (int jc = 0; jc < 4; ++jc) tmem_ld16(tbase + lane_base + db * colw + q * 64 + jc * 16, r + 16 * jc);
-        tmem_wait_ld();
-        const float4* wq = reinterpret_cast<const float4*>(wsm + q * 64);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float4 wv = wq[e];
-          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * e]), 0.f), acc[0]);
-          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * e + 1]), 0.f), acc[1]);
-          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * e + 2]), 0.f), acc[2]);
-          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * e + 3]), 0.f), acc[3]);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[32];
+          tmem_ld16(tbase + lane_base + db * colw + q * 64 + hf * 32, r);
+          tmem_ld16(tbase + lane_base + db * colw + q * 64 + hf * 32 + 16, r + 16);
+          tmem_wait_ld();
+          const float4* wq = reinterpret_cast<const float4*>(wsm + q * 64) + hf * 8;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 wv = wq[e];
+            acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * e]), 0.f), acc[0]);
+            acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * e + 1]), 0.f), acc[1]);
+            acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * e + 2]), 0.f), acc[2]);
+            acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * e + 3]), 0.f), acc[3]);
+          }
         }
         if (s < nq)
           p.out[static_cast<size_t>(it.t0 + q) * p.ld + s] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
@@ -424,24 +442,28 @@ __device__ void ix_epilogue(const IndexerParams& p, const IxCtx& c, uint32_t tba
   }
 }
 
-__global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_constant__ IndexerParams p) {
+template <int NG>
+__global__ void __launch_bounds__(IxWarps<NG>::kThreads, 1)
+    indexer_kernel(const __grid_constant__ IndexerParams p) {
+  using W = IxWarps<NG>;
+  constexpr int kOffMisc = IxLayout<NG>::kOffMisc;
   extern __shared__ uint8_t ix_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ix_smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   IxCtx c;
   c.sbase = smem_u32(sm);
-  c.abort_flag = reinterpret_cast<volatile uint32_t*>(sm + IX_OFF_MISC + 16);
+  c.abort_flag = reinterpret_cast<volatile uint32_t*>(sm + kOffMisc + 16);
   c.status = p.status;
   if (threadIdx.x == 0) {
     *c.abort_flag = 0u;
     for (int b = 0; b < p.stages; ++b) {
       mbar_init(c.bar(IB_K_FULL + b), 1);
-      mbar_init(c.bar(IB_K_EMPTY + b), 8);
+      mbar_init(c.bar(IB_K_EMPTY + b), W::kEpi);
     }
     for (int b = 0; b < 8; ++b) {
       mbar_init(c.bar(IB_D_FULL + b), 1);
-      mbar_init(c.bar(IB_D_EMPTY + b), 256);
+      mbar_init(c.bar(IB_D_EMPTY + b), 128 * NG);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(c.bar(IB_Q_FULL + b), 1);
@@ -451,19 +473,19 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
     mbar_init(c.bar(IB_NEVER), 1);
     fence_mbar_init_cluster();
   }
-  if (warp == 9) {
-    tmem_alloc(c.sbase + IX_OFF_MISC, 512);
+  if (warp == W::kMma) {
+    tmem_alloc(c.sbase + kOffMisc, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + IX_OFF_MISC);
-  if (warp < 8) {
-    ix_epilogue(p, c, tbase, threadIdx.x & 127, warp >> 2,
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sm + kOffMisc);
+  if (warp < W::kEpi) {
+    ix_epilogue<NG>(p, c, tbase, threadIdx.x & 127, warp >> 2,
                 reinterpret_cast<float*>(sm + IX_OFF_W) + warp * 256,
                 reinterpret_cast<const float*>(sm + p.off_sc));
-  } else if (warp == 8) {
+  } else if (warp == W::kProducer) {
     ix_producer(p, c, lane);
   } else if (lane == 0) {
     ix_mma(p, c, tbase);
@@ -476,7 +498,7 @@ __global__ void __launch_bounds__(IX_THREADS, 1) indexer_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tbase, 512);
+  if (warp == W::kMma) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
@@ -513,21 +535,25 @@ cudaError_t launch_indexer(const IndexerLaunch& L, cudaStream_t stream) {
   // stages: as many as fit beside the two Q buffers (at least 116 KB in all, so that one CTA
   // holds an SM: each CTA allocates all 512 tensor-memory columns)
   p.q_bytes = static_cast<uint32_t>(p.G) * 64 * 128;
+  const bool three = p.G > 1;  // three epilogue warpgroups when a group has several tokens
+  p.off_stages = static_cast<uint32_t>(three ? IxLayout<3>::kOffStages : IxLayout<2>::kOffStages);
   uint32_t smem = 0;
   for (p.stages = IX_MAX_STAGES; p.stages > 2; --p.stages) {
-    p.off_sc = IX_OFF_STAGES + p.stages * IX_STAGE_BYTES;
+    p.off_sc = p.off_stages + p.stages * IX_STAGE_BYTES;
     p.off_q = (p.off_sc + p.stages * IX_SC_BYTES + 1023u) & ~1023u;
     smem = p.off_q + 2 * p.q_bytes + 1024;  // + slack to align the base
     if (smem <= static_cast<uint32_t>(IX_SMEM_MAX)) break;
   }
   if (smem < 116u * 1024) smem = 116u * 1024;
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kernel)(IndexerParams) = three ? indexer_kernel<3> : indexer_kernel<2>;
+  const int threads = three ? IxWarps<3>::kThreads : IxWarps<2>::kThreads;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int64_t total_tiles = static_cast<int64_t>(p.n_groups) * p.max_tiles;
   int grid = total_tiles < L.num_sms ? static_cast<int>(total_tiles) : L.num_sms;
   if (grid < 1) grid = 1;
-  indexer_kernel<<<grid, IX_THREADS, smem, stream>>>(p);
+  kernel<<<grid, threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
