@@ -91,6 +91,27 @@ def test_topk_signed_zero_and_infinities(dev, dtype):
     _check(out, scores, lens, table, 1, k)
 
 
+@pytest.mark.parametrize("n_tok", [4, 96])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shift,k", [(-5.0, 2048), (0.0, 12288), (0.0, 19661), (3.0, 100)])
+def test_topk_boundary_sign(dev, dtype, shift, k, n_tok):
+    # where the sampled boundary falls decides how the full pass tests a candidate: on its raw
+    # bits when the boundary is non-negative, on its key otherwise.  All-negative rows, a
+    # boundary near zero (half the row selected), one below zero (80 %) and a high one.
+    ld = 24576
+    g = torch.Generator().manual_seed(int(k + 10 * shift))
+    base = torch.randn(n_tok, ld, generator=g) + shift
+    base[:, ::97] = 0.0
+    base[:, 1::89] = -0.0
+    scores = base.to(dtype).to(dev)
+    lens = torch.tensor([ld, ld - 3, k + 1000, ld // 2 + 17] * (n_tok // 4), dtype=torch.int32,
+                        device=dev)
+    table = _table(n_tok, ld // 64, seed=9, dev=dev)
+    out = smla.topk_page_table(scores, lens, table, 1, k)
+    torch.cuda.synchronize()
+    _check(out, scores, lens, table, 1, k)
+
+
 def test_topk_strided_rows_and_table_flag(dev):
     n_tok, ld, k = 4, 8192, 512
     big = workloads.index_scores(n_tok, ld + 64, torch.bfloat16, seed=5, device=dev)
