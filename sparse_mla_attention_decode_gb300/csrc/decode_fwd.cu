@@ -75,8 +75,8 @@ enum Bar {
   B_DRAIN = B_O_EMPTY + 1,          // MMA drain on the way out
   B_STAGED = B_DRAIN + 1,           // [NMSG] 128 softmax threads wrote a message slot (S-CTA)
   B_QLOAD = B_STAGED + NMSG,        // [9] 1 expect-tx arrival + the bytes of one Q chunk
-  B_QREAD = B_QLOAD + 9,            // 128 softmax threads: Q read out of the key-tile region
-  B_OSTAGE = B_QREAD + 1,           // [8] 128 epilogue threads staged one output box (O-CTA)
+  B_QREAD = B_QLOAD + 9,            // [2] 128 softmax threads: Q read out of key-tile stage 0 / 1
+  B_OSTAGE = B_QREAD + 2,           // [8] 128 epilogue threads staged one output box (O-CTA)
   B_OFREE = B_OSTAGE + 8,           // the stores have read the staging tiles (O-CTA)
   B_LAST = B_OFREE + 1,             // one-shot commit after the partition's final PV (O-CTA)
   B_NEVER = B_LAST + 1,             // nothing arrives here (the test_stall hook waits on it)
@@ -539,7 +539,8 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
     // each token's Q passes through the key-tile region on its way to tensor memory: the
     // first tile of a request waits until it has been read out
-    if (kScores && cur.blk == pl.first_block(cur.req) && !c.wait_warp(B_QREAD, cur.item & 1u))
+    if (kScores && cur.blk - pl.first_block(cur.req) < NSTAGE &&
+        !c.wait_warp(B_QREAD + st, cur.item & 1u))
       goto out;
     {
       const uint32_t tile = c.sbase + OFF_TILE + st * stage_bytes;
@@ -664,7 +665,9 @@ __device__ void role_mma_values(const Ctx& c, const Plan& pl, uint32_t tbase) {
 // per 64-dim chunk, h_q rows of 128 bytes, 128-byte swizzle), each with its own barrier, into
 // the key-tile region; thread i = head i converts its row to fp16 into tensor memory chunk by
 // chunk as the copies land.  The region is free then: every QK of the previous request has
-// completed and the dequant warps hold the request's first tile back until B_QREAD.  The
+// completed and the dequant warps hold the request's first two tiles back until B_QREAD of
+// their stage (stage 0's part of Q is read out first, so the first tile can be written while
+// the rest converts).  The
 // swizzle puts unit u of row r at position u ^ (r % 8), so eight consecutive heads read eight
 // distinct bank groups.  The fp16 range is checked on the bf16 magnitudes (a packed 16-bit
 // max), not per converted value: the conversion is issue-bound on the SM sub-partitions.
@@ -690,6 +693,11 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
   const bool live = i < p.h_q;
   const uint32_t row = qs + static_cast<uint32_t>(i) * 128;
   const uint32_t sw = static_cast<uint32_t>(i & 7);
+  // the chunks overlapping each key-tile stage: stage 0 is free once chunk lo_last is read,
+  // stage 1 once the last chunk is (or at once when Q does not reach it)
+  const int lo_last = min(nch, static_cast<int>((KT_STAGE + chunk_bytes - 1) / chunk_bytes)) - 1;
+  const bool reaches_hi = static_cast<uint32_t>(nch) * chunk_bytes > KT_STAGE;
+  if (!reaches_hi) mbar_arrive(c.bar(B_QREAD + 1));
   uint32_t mag[4] = {0u, 0u, 0u, 0u};  // largest bf16 magnitude seen, per 16-bit half (4 chains)
 #pragma unroll 1
   for (int ch = 0; ch < nch; ++ch) {
@@ -712,6 +720,7 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
     }
     tmem_st16(tq + ch * 32, w);
     tmem_st16(tq + ch * 32 + 16, w + 16);
+    if (ch == lo_last) mbar_arrive(c.bar(B_QREAD));  // this thread is done with stage 0
   }
   // bf16 magnitude 0x4780 (2^16) and above rounds to inf in fp16 (0x477F = 65280 is finite)
   const uint32_t m = vmax_u16x2(vmax_u16x2(mag[0], mag[1]), vmax_u16x2(mag[2], mag[3]));
@@ -719,7 +728,7 @@ __device__ bool stage_q_bulk(const DecodeParams& p, const Ctx& c, uint32_t tq, i
   tmem_wait_st();
   tc_fence_before();
   mbar_arrive(c.bar(B_Q_FULL));
-  mbar_arrive(c.bar(B_QREAD));  // this thread is done with the key-tile region
+  if (reaches_hi) mbar_arrive(c.bar(B_QREAD + 1));  // and with stage 1
   return true;
 }
 
@@ -1167,7 +1176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(c.bar(B_Q_FULL), 128);
     for (int b = 0; b < 9; ++b) mbar_init(c.bar(B_QLOAD + b), 1);
-    mbar_init(c.bar(B_QREAD), 128);
+    for (int b = 0; b < NSTAGE; ++b) mbar_init(c.bar(B_QREAD + b), 128);
     for (int b = 0; b < 8; ++b) mbar_init(c.bar(B_OSTAGE + b), 128);
     mbar_init(c.bar(B_OFREE), 1);
     mbar_init(c.bar(B_LAST), 1);
