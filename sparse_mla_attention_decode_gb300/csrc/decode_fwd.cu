@@ -538,7 +538,8 @@ __device__ void role_dequant(const DecodeParams& p, const Ctx& c, const Plan& pl
     vmask |= valid_bits(ixA, extra_next) << 8;
     if (g >= NSTAGE && !c.wait_warp(bempty + st, ((g >> 1) - 1) & 1)) goto out;
     // each token's Q passes through the key-tile region on its way to tensor memory: the
-    // first tile of a request waits until it has been read out
+    // first two tiles of a request (one per stage) wait until their stage's part of it has
+    // been read out
     if (kScores && cur.blk - pl.first_block(cur.req) < NSTAGE &&
         !c.wait_warp(B_QREAD + st, cur.item & 1u))
       goto out;
