@@ -795,7 +795,8 @@ __device__ void role_softmax(const DecodeParams& p, const Ctx& c, const Plan& pl
       const uint32_t sb = g % NSBUF, st = g % NMSG;
       if (!c.wait_warp(B_S_FULL + sb, (g / NSBUF) & 1)) goto out;
       tc_fence_after();
-      // the item's last QK has completed: the next item's Q copies can start now
+      // the item's last QK has completed: the next item's Q copies can start now (every item
+      // has a last block: the plan splits a request only where both sides keep a block)
       if (i == 0 && blk == b1 - 1 && !pl.last_item(s, req)) {
         const int nreq = req < pl.end_req ? req + 1 : pl.begin_req;
         const int ns = req < pl.end_req ? s : s + pl.s_step;
