@@ -358,7 +358,9 @@ def test_scheduler_worked_example():
 
 
 @pytest.mark.parametrize("b,topk,parts", [(64, 2048, 76), (32, 2048, 76), (128, 2048, 38),
-                                          (1, 2048, 1), (3, 100, 7), (5, 0, 4), (200, 64, 3)])
+                                          (1, 2048, 1), (3, 100, 7), (5, 0, 4), (200, 64, 3),
+                                          (7, 1, 76), (2, 65, 76), (33, 4096, 76), (76, 640, 76),
+                                          (9, 2048 + 64 * 7, 37), (1, 64, 76)])
 def test_scheduler_covers_every_block_once(b, topk, parts):
     plan, prefix = osched.plan([topk] * b, parts)
     nb = -(-topk // 64)
@@ -370,7 +372,9 @@ def test_scheduler_covers_every_block_once(b, topk, parts):
             continue
         for r in range(p.begin_req, p.end_req + 1):
             lo, hi = osched.block_range(p, r, nb)
-            assert 0 <= lo <= hi <= nb
+            # every request a partition touches gets at least one of its blocks (the decode
+            # kernel relies on it: each (position, request) item has a last block)
+            assert 0 <= lo < hi <= nb if nb else lo == hi == 0
             seen[r, lo:hi] += 1
             reqs_touched[r] += 1
             slot = p.begin_split_idx if r == p.begin_req else prefix[r]
