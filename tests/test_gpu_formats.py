@@ -35,6 +35,7 @@ def _check(wl, num_sms, what, tokens=None, **kw):
 CASES = [  # (b, s_q, h_q, topk, ctx, masked, num_sms)
     (2, 1, 128, 128, 512, 0, 152),
     (3, 2, 128, 200, 1024, 7, 4),      # several requests per partition, ragged tail
+    (3, 2, 64, 200, 1024, 5, 4),       # the same at h_q = 64 (Q stays in one key-tile stage)
     (2, 1, 64, 300, 2048, 5, 152),     # h_q = 64, requests split over partitions
     (4, 1, 128, 17, 256, 0, 8),        # one short block
     (2, 2, 128, 2048, 8192, 100, 152), # split, full-length list

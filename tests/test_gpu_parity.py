@@ -80,6 +80,9 @@ SMALL = [
     ("b1_h128_k2048_many_splits", dict(b=1, h_q=128, topk=2048, ctx=8192), 152),
     ("b5_h64_k64_oneblock", dict(b=5, h_q=64, topk=64, ctx=512, masked_per_row=10), 152),
     ("b2_h128_k17_tiny", dict(b=2, h_q=128, topk=17, ctx=256), 4),
+    # several query positions per cluster (persistent) and several requests per partition
+    ("b3_sq5_h128_k192_persistent", dict(b=3, s_q=5, h_q=128, topk=192, ctx=1024), 4),
+    ("b3_sq5_h64_k192_persistent", dict(b=3, s_q=5, h_q=64, topk=192, ctx=1024), 4),
 ]
 
 
